@@ -1,0 +1,465 @@
+"""Checks that pin the CPU oracle to facts fixed outside the oracle itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with:
+  * the pages' worked example ("NCCL, NIXL, and Distributed GPU Communication",
+    section "All-reduce": g0 + g1 + g2 + g3 on every GPU, DDP mean = / world_size);
+  * the ring algorithm run literally as message passing: P-1 reduce-scatter
+    steps then P-1 all-gather steps moving chunks between P arrays (same page,
+    section "Reduce-scatter": all-reduce = reduce-scatter + all-gather;
+    lecture_068 page, section 05: the ring takes 2(N-1) steps);
+  * the two binary trees' combination expressions derived by hand (below);
+  * order independence: integer sums (mod 2^32) and min / max give one answer
+    whatever the order, so ring == tree == LL == numpy's plain reduction;
+  * the textbook recursive-summation bound |y - sum| <= (P-1) u sum|x_i|;
+  * exact power-of-two scaling and PyTorch's round-to-nearest-even bf16 cast.
+The functions are shared by test_oracle_pins.py (the real oracle must pass)
+and test_oracle_mutants.py (oracles with planted mistakes must fail one).
+"""
+from __future__ import annotations
+
+import math
+import os
+import re
+
+import numpy as np
+import torch
+
+from oracle import BF16, F32, I32, LL, MAX, MIN, RING, SUM, TREE, NP_DTYPE, OracleError
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+# Hand-derived from the reading of "NCCL and NVSHMEM -- two GPU communication
+# models, side by side", section "double binary tree": labels 1..P in an
+# in-order binary tree rooted at the largest power of two <= P; tree 0 puts
+# rank r at label r+1, tree 1 shifts every rank by one (label v -> rank v mod P);
+# node value = ((own + left) + right).  Worked by hand, e.g. P = 6: root 4 has
+# left 2 (children 1, 3) and right 6 (left child 5, no label 7).
+TREE_EXPRESSIONS = {
+    1: ("x0", "x0"),
+    2: ("(x1+x0)", "(x0+x1)"),
+    3: ("((x1+x0)+x2)", "((x2+x1)+x0)"),
+    4: ("(x3+((x1+x0)+x2))", "(x0+((x2+x1)+x3))"),
+    5: ("((x3+((x1+x0)+x2))+x4)", "((x4+((x2+x1)+x3))+x0)"),
+    6: ("((x3+((x1+x0)+x2))+(x5+x4))", "((x4+((x2+x1)+x3))+(x0+x5))"),
+    7: ("((x3+((x1+x0)+x2))+((x5+x4)+x6))", "((x4+((x2+x1)+x3))+((x6+x5)+x0))"),
+    8: ("(x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))", "(x0+((x4+((x2+x1)+x3))+((x6+x5)+x7)))"),
+}
+
+VEC = {F32: 4, BF16: 8, I32: 4}   # elements per 16-byte vector
+
+
+# ------------------------------------------------------------------ helpers
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def bf16_bits_torch(x: np.ndarray) -> np.ndarray:
+    """RNE fp32 -> bf16 by PyTorch's cast (a library routine, not the oracle's)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def mixed_f32(rng, n: int) -> np.ndarray:
+    """Values whose magnitudes span 2^-12 .. 2^12, so the fold order shows."""
+    sign = rng.choice([-1.0, 1.0], size=n)
+    e = rng.integers(-12, 13, size=n)
+    return (sign * np.ldexp(1.0 + rng.random(n), e)).astype(np.float32)
+
+
+def random_inputs(rng, P: int, count: int, dtype: int):
+    if dtype == F32:
+        return [mixed_f32(rng, count) for _ in range(P)]
+    if dtype == BF16:
+        return [bf16_bits_torch(mixed_f32(rng, count)) for _ in range(P)]
+    return [rng.integers(-2**31, 2**31, size=count, dtype=np.int64).astype(np.int32)
+            for _ in range(P)]
+
+
+def widened(a: np.ndarray, dtype: int):
+    """Python-level scalars: np.float32 for fp32 / bf16, int for int32."""
+    if dtype == BF16:
+        return list(bf16_value(a))
+    if dtype == F32:
+        return list(a)
+    return [int(v) for v in a]
+
+
+def combine(acc, x, dtype: int, op: int):
+    """acc (+) x exactly as the pages' ops define it, in the stated tie rule."""
+    if dtype == I32:
+        if op == SUM:
+            s = (acc + x) & 0xFFFFFFFF
+            return s - (1 << 32) if s >= (1 << 31) else s
+        if op == MIN:
+            return x if x < acc else acc
+        return x if x > acc else acc
+    if op == SUM:
+        return np.float32(acc) + np.float32(x)
+    if op == MIN:
+        return x if x < acc else acc
+    return x if x > acc else acc
+
+
+def narrow(vals, dtype: int, scale: float):
+    if dtype == I32:
+        return np.array(vals, dtype=np.int64).astype(np.int32)
+    f = np.array(vals, dtype=np.float32)
+    if scale != 1.0:
+        f = f * np.float32(scale)
+    if dtype == BF16:
+        return bf16_bits_torch(f)
+    return f
+
+
+def assert_bitwise(a: np.ndarray, b: np.ndarray, what: str):
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    if not np.array_equal(a.view(np.uint8), b.view(np.uint8)):
+        bad = np.nonzero(a != b)[0][:5]
+        raise AssertionError(f"{what}: differs at {bad.tolist()}: {a[bad]} vs {b[bad]}")
+
+
+# ------------------------------------------------------------ ring by steps
+
+def ring_message_passing(sends, dtype: int, op: int, scale: float):
+    """The ring all-reduce run literally: chunks travel between P buffers.
+
+    Reduce-scatter: at step s (0 .. P-2) rank r sends its partial of chunk
+    (r - s) mod P to rank r+1, which combines (incoming partial) (+) (own).
+    After P-1 steps chunk c is complete at rank c-1, which applies the scale
+    and narrowing.  All-gather: at step s rank r forwards chunk (r + 1 - s)
+    mod P to rank r+1, which stores it.  Chunks are P equal pieces whose
+    length is rounded up to a 16-byte multiple (trailing pieces may be empty).
+    """
+    P = len(sends)
+    count = len(sends[0])
+    L = ceil_div(ceil_div(count, P), VEC[dtype]) * VEC[dtype]
+    bounds = [(min(count, c * L), min(count, (c + 1) * L)) for c in range(P)]
+    buf = [widened(s, dtype) for s in sends]
+    for s in range(P - 1):
+        msgs = []
+        for r in range(P):
+            c = (r - s) % P
+            lo, hi = bounds[c]
+            msgs.append(((r + 1) % P, c, buf[r][lo:hi]))
+        for dst, c, data in msgs:
+            lo, hi = bounds[c]
+            for i, e in enumerate(range(lo, hi)):
+                buf[dst][e] = combine(data[i], buf[dst][e], dtype, op)
+    out = [None] * P
+    for r in range(P):
+        out[r] = np.zeros(count, dtype=NP_DTYPE[dtype])
+    final = [None] * P   # narrowed chunk c, held by its owner
+    for c in range(P):
+        lo, hi = bounds[c]
+        final[c] = narrow(buf[(c - 1) % P][lo:hi], dtype, scale)
+    held = [{(r + 1) % P: final[(r + 1) % P]} for r in range(P)]
+    for s in range(P - 1):
+        msgs = []
+        for r in range(P):
+            c = (r + 1 - s) % P
+            msgs.append(((r + 1) % P, c, held[r][c]))
+        for dst, c, data in msgs:
+            held[dst][c] = data
+    for r in range(P):
+        assert len(held[r]) == P, "all-gather did not reach every rank"
+        for c in range(P):
+            lo, hi = bounds[c]
+            out[r][lo:hi] = held[r][c]
+    return out
+
+
+# ---------------------------------------------------------- tree expressions
+
+def eval_expr(expr: str, xs, dtype: int, op: int):
+    """Evaluates a '(a+b)' expression over x0..x{P-1} with combine()."""
+    pos = 0
+
+    def parse():
+        nonlocal pos
+        if expr[pos] == "(":
+            pos += 1
+            a = parse()
+            assert expr[pos] == "+"
+            pos += 1
+            b = parse()
+            assert expr[pos] == ")"
+            pos += 1
+            return combine(a, b, dtype, op)
+        m = re.match(r"x(\d+)", expr[pos:])
+        pos += m.end()
+        return xs[int(m.group(1))]
+
+    v = parse()
+    assert pos == len(expr)
+    return v
+
+
+def expr_structure(expr: str):
+    """(ranks in order of appearance, ranks that have children)."""
+    ranks = [int(m) for m in re.findall(r"x(\d+)", expr)]
+    interior = {int(m) for m in re.findall(r"\(x(\d+)\+", expr)}
+    return ranks, interior
+
+
+# ------------------------------------------------------------------- pins
+
+def pin_worked_example(O):
+    """Golden: "NCCL, NIXL, and Distributed GPU Communication", section "All-reduce"."""
+    spec = {"before": {}, "after": {}}
+    nranks = None
+    with open(os.path.join(GOLDEN, "worked_example_allreduce_p4.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *rest = line.split()
+            if key == "ranks":
+                nranks = int(rest[0])
+            else:
+                spec[key][int(rest[0])] = rest[1]
+    assert nranks == 4 and len(spec["before"]) == 4 and len(spec["after"]) == 4
+    rng = np.random.default_rng(2024)
+    count = 4096 + 3
+    for dtype, lim in ((F32, 1 << 20), (I32, 1 << 20), (BF16, 32)):
+        ints = {spec["before"][r]: rng.integers(-lim, lim + 1, size=count) for r in range(4)}
+        sends = []
+        for r in range(4):
+            v = ints[spec["before"][r]]
+            if dtype == BF16:
+                sends.append(bf16_bits_torch(v.astype(np.float32)))
+            else:
+                sends.append(v.astype(NP_DTYPE[dtype]))
+        for algo in (RING, TREE, LL):
+            scales = (1.0, 0.25) if dtype != I32 else (1.0,)
+            for scale in scales:
+                outs = O.allreduce(sends, dtype, SUM, algo, scale)
+                for r in range(4):
+                    terms = spec["after"][r].split("+")
+                    exact = sum(ints[t] for t in terms)           # Python integers
+                    if dtype == I32:
+                        want = exact.astype(np.int32)
+                    else:
+                        want = (exact.astype(np.float64) * scale).astype(np.float32)
+                        if dtype == BF16:
+                            want = bf16_bits_torch(want)
+                    assert_bitwise(outs[r], want, f"worked example dtype={dtype} algo={algo} "
+                                                  f"scale={scale} rank={r}")
+
+
+def pin_outputs_identical(O):
+    """Every rank's receive buffer holds the same result (section "All-reduce")."""
+    rng = np.random.default_rng(7)
+    for P in (1, 2, 3, 5, 8, 13):
+        for count in (0, 1, 7, 33, 100):
+            for dtype in (F32, BF16, I32):
+                sends = random_inputs(rng, P, count, dtype)
+                for op in (SUM, MIN, MAX):
+                    for algo in (RING, TREE, LL):
+                        outs = O.allreduce(sends, dtype, op, algo)
+                        for r in range(1, P):
+                            assert_bitwise(outs[r], outs[0], f"rank {r} vs rank 0 P={P} "
+                                                             f"count={count} algo={algo}")
+
+
+def pin_ring_simulation(O, quick: bool = False):
+    rng = np.random.default_rng(11)
+    Ps = (1, 2, 3, 4, 5, 7, 8, 9) if not quick else (1, 3, 4, 8)
+    counts = (0, 1, 3, 4, 5, 8, 17, 31, 40) if not quick else (1, 5, 17, 40)
+    for P in Ps:
+        for count in counts:
+            for dtype in (F32, BF16, I32):
+                sends = random_inputs(rng, P, count, dtype)
+                for op in (SUM, MIN, MAX):
+                    scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                    for scale in scales:
+                        want = ring_message_passing(sends, dtype, op, scale)
+                        for algo in (RING, LL):
+                            got = O.allreduce(sends, dtype, op, algo, scale)
+                            for r in range(P):
+                                assert_bitwise(got[r], want[r],
+                                               f"ring sim P={P} count={count} dtype={dtype} "
+                                               f"op={op} scale={scale} algo={algo} rank={r}")
+
+
+def pin_tree_expressions(O):
+    rng = np.random.default_rng(5)
+    for P, exprs in TREE_EXPRESSIONS.items():
+        for t in (0, 1):
+            got = O.tree_expr(P, t)
+            assert got == exprs[t], f"tree {t} for P={P}: {got} != {exprs[t]}"
+        # numeric: the hand-derived expressions, evaluated in fp32, give the
+        # oracle's tree all-reduce on both halves of the buffer
+        # (count 65: ceil(count/2) and floor(count/2) round up to different splits)
+        for dtype in (F32, BF16):
+            for count in (65, 69, 3):
+                sends = random_inputs(rng, P, count, dtype)
+                V = VEC[dtype]
+                H = min(count, ceil_div(ceil_div(count, 2), V) * V)
+                outs = O.allreduce(sends, dtype, SUM, TREE)
+                xs = [widened(s, dtype) for s in sends]
+                want = []
+                for e in range(count):
+                    expr = exprs[0] if e < H else exprs[1]
+                    want.append(eval_expr(expr, [x[e] for x in xs], dtype, SUM))
+                assert_bitwise(outs[0], narrow(want, dtype, 1.0),
+                               f"tree numeric P={P} dtype={dtype} count={count}")
+
+
+def pin_tree_structure(O):
+    for P in range(1, 73):
+        interiors = []
+        for t in (0, 1):
+            ranks, interior = expr_structure(O.tree_expr(P, t))
+            assert sorted(ranks) == list(range(P)), f"P={P} tree {t}: ranks {ranks}"
+            interiors.append(interior)
+        if P % 2 == 0:
+            # complementary trees: each rank is interior in exactly one tree
+            assert not (interiors[0] & interiors[1]), f"P={P}: {interiors}"
+            assert interiors[0] | interiors[1] == set(range(P)), f"P={P}: {interiors}"
+
+
+def pin_signed_zero_ties(O):
+    """Min / max keep the earlier operand of a +0 / -0 tie, in fold order.
+
+    Worked by hand from the orders above, fp32, count 8 (two 4-element
+    vectors).  P = 2, x0 = +0, x1 = -0: the ring's chunk 0 starts at rank 0
+    and keeps +0, chunk 1 starts at rank 1 and keeps -0; the tree's first
+    half is (x1 + x0) and keeps -0, its second half (x0 + x1) keeps +0.
+    P = 4, x3 = -0, others +0: tree 0 = (x3 + (...)) keeps -0 on the first
+    half, tree 1 = (x0 + (...)) keeps +0 on the second.
+    """
+    pz, nz = np.float32(0.0), np.float32(-0.0)
+    p2 = [np.full(8, pz, np.float32), np.full(8, nz, np.float32)]
+    p4 = [np.full(8, pz, np.float32)] * 3 + [np.full(8, nz, np.float32)]
+    first_p, first_n = np.array([pz] * 4 + [nz] * 4), np.array([nz] * 4 + [pz] * 4)
+    for op in (MIN, MAX):
+        assert_bitwise(O.allreduce(p2, F32, op, RING)[0], first_p, f"P=2 ring tie op={op}")
+        assert_bitwise(O.allreduce(p2, F32, op, LL)[0], first_p, f"P=2 LL tie op={op}")
+        assert_bitwise(O.allreduce(p2, F32, op, TREE)[0], first_n, f"P=2 tree tie op={op}")
+        assert_bitwise(O.allreduce(p4, F32, op, TREE)[0], first_n, f"P=4 tree tie op={op}")
+
+
+def pin_order_independent(O):
+    rng = np.random.default_rng(13)
+    for P in (1, 2, 3, 8, 9, 72):
+        for count in (1, 9, 257):
+            sends = random_inputs(rng, P, count, I32)
+            wide = np.stack([s.astype(np.int64) for s in sends])
+            s = wide.sum(axis=0) & 0xFFFFFFFF
+            s = np.where(s >= 2**31, s - 2**32, s).astype(np.int32)
+            naive = {SUM: s, MIN: wide.min(axis=0).astype(np.int32),
+                     MAX: wide.max(axis=0).astype(np.int32)}
+            for op in (SUM, MIN, MAX):
+                for algo in (RING, TREE, LL):
+                    assert_bitwise(O.allreduce(sends, I32, op, algo)[0], naive[op],
+                                   f"int32 op={op} algo={algo} P={P}")
+            for dtype in (F32, BF16):
+                sends = random_inputs(rng, P, count, dtype)
+                stack = np.stack(sends)
+                vals = stack if dtype == F32 else bf16_value(stack)
+                for op, red in ((MIN, np.min), (MAX, np.max)):
+                    want = red(vals, axis=0)
+                    if dtype == BF16:
+                        want = bf16_bits_torch(want)
+                    for algo in (RING, TREE, LL):
+                        assert_bitwise(O.allreduce(sends, dtype, op, algo)[0], want,
+                                       f"dtype={dtype} op={op} algo={algo} P={P}")
+
+
+def pin_error_bound(O):
+    """|y - sum x_i| <= (P-1) u sum |x_i| (+ the final bf16 rounding)."""
+    rng = np.random.default_rng(17)
+    u = 2.0 ** -24
+    for P in (2, 4, 8, 16, 72):
+        count = 513
+        for dtype in (F32, BF16):
+            sends = random_inputs(rng, P, count, dtype)
+            x = np.stack([s if dtype == F32 else bf16_value(s) for s in sends]).astype(np.float64)
+            exact = x.sum(axis=0)                          # exact: few terms, wide range ok
+            mag = np.abs(x).sum(axis=0)
+            bound = (P - 1) * u * mag * (1 + 1e-6)
+            for algo in (RING, TREE, LL):
+                y = O.allreduce(sends, dtype, SUM, algo)[0]
+                yv = (y if dtype == F32 else bf16_value(y)).astype(np.float64)
+                b = bound if dtype == F32 else bound + 2.0 ** -8 * (np.abs(exact) + bound)
+                err = np.abs(yv - exact)
+                assert np.all(err <= b), f"bound P={P} dtype={dtype} algo={algo} " \
+                                         f"worst {np.max(err - b)}"
+    # and the bound is not vacuous: the ring order and the tree order do
+    # differ somewhere on these inputs (so the order is really being applied)
+    sends = random_inputs(rng, 8, 4096, F32)
+    ring = O.allreduce(sends, F32, SUM, RING)[0]
+    tree = O.allreduce(sends, F32, SUM, TREE)[0]
+    assert not np.array_equal(ring, tree), "ring and tree orders gave identical fp32 sums"
+
+
+def pin_scale(O):
+    """DDP mean (section "All-reduce"): a power-of-two scale is exact."""
+    rng = np.random.default_rng(19)
+    for P in (2, 8):
+        for dtype in (F32, BF16):
+            sends = random_inputs(rng, P, 300, dtype)
+            for algo in (RING, TREE, LL):
+                y1 = O.allreduce(sends, dtype, SUM, algo, 1.0)[0]
+                y8 = O.allreduce(sends, dtype, SUM, algo, 0.125)[0]
+                if dtype == F32:
+                    assert_bitwise(y8, (y1 * np.float32(0.125)).astype(np.float32), "scale f32")
+                else:
+                    assert_bitwise(y8, bf16_bits_torch(bf16_value(y1) * np.float32(0.125)),
+                                   "scale bf16")
+    sends = random_inputs(rng, 2, 10, I32)
+    for bad in ((I32, SUM), (F32, MIN), (F32, MAX), (BF16, MAX)):
+        dsends = sends if bad[0] == I32 else random_inputs(rng, 2, 10, bad[0])
+        try:
+            O.allreduce(dsends, bad[0], bad[1], RING, 0.5)
+        except OracleError:
+            continue
+        raise AssertionError(f"scale accepted for dtype={bad[0]} op={bad[1]}")
+
+
+def pin_bf16_rne(O):
+    """Round-to-nearest-even against PyTorch's cast and hand-checked constants."""
+    cases = [(1.0, 0x3F80), (1.0 + 2.0 ** -8, 0x3F80), (1.0 + 3 * 2.0 ** -8, 0x3F82),
+             (-1.0 - 2.0 ** -8 - 2.0 ** -20, 0xBF81), (65504.0, 0x4780), (0.0, 0),
+             (-0.0, 0x8000), (3.0e38, 0x7F62), (3.4e38, 0x7F80)]
+    for x, want in cases:
+        assert O.f32_to_bf16(x) == want, f"RNE({x}) = {O.f32_to_bf16(x):#x}, want {want:#x}"
+    rng = np.random.default_rng(23)
+    xs = np.concatenate([
+        mixed_f32(rng, 3000),
+        # exact halfway points between neighbouring finite bf16 values, both signs
+        ((rng.integers(0, 0x7F80, size=2000).astype(np.uint32)
+          | (rng.integers(0, 2, size=2000).astype(np.uint32) << 15)) << 16 | 0x8000
+         ).astype(np.uint32).view(np.float32),
+        rng.standard_normal(2000).astype(np.float32) * np.float32(1e-30),
+    ])
+    want = bf16_bits_torch(xs)
+    got = np.array([O.f32_to_bf16(float(v)) for v in xs], dtype=np.uint16)
+    assert_bitwise(got, want, "oracle RNE vs torch bf16 cast")
+
+
+def pin_sampled_matches_full(O):
+    rng = np.random.default_rng(29)
+    for P, count, dtype in ((8, 1003, F32), (8, 2050, BF16), (72, 400, I32), (3, 70, F32)):
+        sends = random_inputs(rng, P, count, dtype)
+        idx = np.unique(np.concatenate([[0, count - 1], rng.integers(0, count, 50)]))
+        vals = np.stack([s[idx] for s in sends])
+        for algo in (RING, TREE):
+            ops = (SUM, MIN, MAX)
+            for op in ops:
+                full = O.allreduce(sends, dtype, op, algo)[0]
+                assert_bitwise(O.allreduce_sampled(vals, idx, count, dtype, op, algo),
+                               full[idx], f"sampled P={P} dtype={dtype} algo={algo} op={op}")
+
+
+ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_tree_expressions,
+            pin_tree_structure, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
+            pin_sampled_matches_full]

@@ -1,0 +1,68 @@
+"""Planted mistakes in the oracle must fail at least one pin (no GPU).
+
+Each mutant is a copy of oracle.c with one plausible slip -- a dropped term,
+a wrong index or sign, a transposed operand, a wrong rounding tie -- compiled
+into a scratch directory.  A mutant that passes every pin would mean the pins
+cannot tell that slip from the real oracle.
+"""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = {
+    "ring_direction": ("x[(c + k) % P]", "x[(c + P - k) % P]"),
+    "ring_start_rank": ("int c = (int)(e / L);", "int c = (int)((e / L + 1) % (size_t)P);"),
+    "ring_dropped_rank": ("for (int k = 1; k < P; ++k)", "for (int k = 1; k < P - 1; ++k)"),
+    "chunk_not_16B": ("return round_up(per, vec_elems(dtype));", "return per;"),
+    "sum_sign": ("acc.f = acc.f + x.f;", "acc.f = acc.f - x.f;"),
+    "min_flipped": ("acc.f = (x.f < acc.f) ? x.f : acc.f;", "acc.f = (x.f > acc.f) ? x.f : acc.f;"),
+    "int_min_unsigned": ("acc.u = (uint32_t)((b < a) ? b : a);",
+                         "acc.u = (x.u < acc.u) ? x.u : acc.u;"),
+    "tree_children_swapped": (
+        "    if (l) acc = combine(acc, tree_value(x, l, P, t, dtype, op), dtype, op);\n"
+        "    if (r) acc = combine(acc, tree_value(x, r, P, t, dtype, op), dtype, op);",
+        "    if (r) acc = combine(acc, tree_value(x, r, P, t, dtype, op), dtype, op);\n"
+        "    if (l) acc = combine(acc, tree_value(x, l, P, t, dtype, op), dtype, op);"),
+    "tree_own_last": (
+        "    acc_t acc = x[tree_owner(v, P, t)];\n    int l = tree_left(v), r = tree_right(v, P);\n"
+        "    if (l) acc = combine(acc, tree_value(x, l, P, t, dtype, op), dtype, op);",
+        "    int l = tree_left(v), r = tree_right(v, P);\n"
+        "    acc_t acc = l ? tree_value(x, l, P, t, dtype, op) : x[tree_owner(v, P, t)];\n"
+        "    if (l) acc = combine(acc, x[tree_owner(v, P, t)], dtype, op);"),
+    "tree1_shift_wrong": ("return t == 0 ? v - 1 : v % P;", "return t == 0 ? v - 1 : (v + 1) % P;"),
+    "tree_right_dropped": ("if (r) acc = combine(acc, tree_value(x, r, P, t, dtype, op), dtype, op);",
+                           "(void)r;"),
+    "tree_split_floor": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
+                         "size_t h = round_up(count / 2, vec_elems(dtype));"),
+    "rne_ties_away": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;",
+                      "if (lower >= 0x8000u) upper += 1;"),
+    "scale_dropped": ("if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;", ""),
+    "only_rank0_written": ("for (int r = 0; r < P; ++r) store_narrowed(recv[r], e, y, dtype);",
+                           "store_narrowed(recv[0], e, y, dtype);"),
+    "bf16_widen_shift": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(before) == 1, f"mutation anchor for {name} not found exactly once"
+    mutant_c = tmp_path / f"{name}.c"
+    mutant_c.write_text(src.replace(before, after))
+    lib = oracle.compile_source(str(mutant_c), str(tmp_path / f"lib{name}.so"))
+    O = oracle.Oracle(lib)
+    failures = []
+    for pin in pins.ALL_PINS:
+        try:
+            if pin is pins.pin_ring_simulation:
+                pin(O, quick=True)
+            else:
+                pin(O)
+        except (AssertionError, oracle.OracleError) as exc:
+            failures.append(f"{pin.__name__}: {str(exc)[:80]}")
+    assert failures, f"mutant {name} passed every pin"
+    os.remove(lib)
