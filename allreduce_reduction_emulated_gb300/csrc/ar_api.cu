@@ -1,0 +1,307 @@
+// ar_api.cu -- the C ABI of libar.so (declared in include/ar.h): communicator
+// lifetime, argument checks, algorithm selection and kernel dispatch.
+// Host code only; the kernels live in ar_static_*.cu, ar_generic.cu, ar_ll.cu.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/ar.h"
+#include "ar_device.cuh"
+#include "ar_launch.h"
+
+struct ar_comm {
+  int P = 0;
+  int device = 0;
+  int sms = 0;
+  // LL staging: P slots of `stage_stride` 8-byte words (one word per 4 payload bytes)
+  unsigned long long* staging = nullptr;
+  size_t stage_stride = 0;
+  size_t ll_capacity_bytes = 0;  // per rank, fixed at ar_init
+  size_t ll_max_bytes = 0;       // current AUTO threshold / LL limit (<= capacity)
+  uint32_t epoch = 0;            // last epoch used; 0 never appears in a staged word
+  uint32_t spin_limit = 0;
+  int skip_produce = 0;
+  int debug = 0;
+  int* status = nullptr;         // device ar_status_t word
+  int16_t* tree_prog = nullptr;  // device: tree 0 program then tree 1 program
+  int prog_len = 0;
+};
+
+namespace {
+
+constexpr size_t kDefaultLLBytes = 65536;
+constexpr uint32_t kDefaultSpinLimit = 1u << 22;  // ~1 s of L2 polls at worst
+constexpr size_t kMaxLLBytes = 1u << 20;
+
+long long env_ll(const char* name, long long dflt) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return dflt;
+  char* end = nullptr;
+  long long v = std::strtoll(s, &end, 0);
+  return (end && *end == 0) ? v : dflt;
+}
+
+bool valid_dtype(int d) { return d == AR_FLOAT32 || d == AR_BFLOAT16 || d == AR_INT32; }
+bool valid_op(int o) { return o == AR_SUM || o == AR_MIN || o == AR_MAX; }
+bool valid_algo(int a) {
+  return a == AR_ALGO_AUTO || a == AR_ALGO_RING || a == AR_ALGO_TREE || a == AR_ALGO_LL;
+}
+
+// Postorder program of tree t: push own rank, then each child's subtree
+// followed by a combine -- i.e. ((own (+) left) (+) right).
+void emit_tree(int v, int P, int t, std::vector<int16_t>& out) {
+  out.push_back((int16_t)ar::tree_owner(v, P, t));
+  const int l = ar::tree_left(v), r = ar::tree_right(v, P);
+  if (l) {
+    emit_tree(l, P, t, out);
+    out.push_back(-1);
+  }
+  if (r) {
+    emit_tree(r, P, t, out);
+    out.push_back(-1);
+  }
+}
+
+int program_depth(const std::vector<int16_t>& prog) {
+  int sp = 0, depth = 0;
+  for (int16_t op : prog) {
+    sp += op >= 0 ? 1 : -1;
+    depth = std::max(depth, sp);
+  }
+  return depth;
+}
+
+const char* dtype_name(int d) { return d == AR_FLOAT32 ? "f32" : d == AR_BFLOAT16 ? "bf16" : "i32"; }
+const char* op_name(int o) { return o == AR_SUM ? "sum" : o == AR_MIN ? "min" : "max"; }
+const char* algo_name(int a) {
+  return a == AR_ALGO_RING ? "ring" : a == AR_ALGO_TREE ? "tree" : a == AR_ALGO_LL ? "ll" : "auto";
+}
+
+void release(ar_comm* c) {
+  if (!c) return;
+  if (c->staging) cudaFree(c->staging);
+  if (c->status) cudaFree(c->status);
+  if (c->tree_prog) cudaFree(c->tree_prog);
+  delete c;
+}
+
+ar_algo_t resolve(const ar_comm* c, size_t count, ar_dtype_t dtype, ar_algo_t algo) {
+  if (algo != AR_ALGO_AUTO) return algo;
+  const size_t bytes = count * ar::elem_bytes(dtype);
+  return bytes <= c->ll_max_bytes ? AR_ALGO_LL : AR_ALGO_RING;
+}
+
+// Rejects buffers that overlap without starting at the same address.  All 2P
+// buffers have the same length, so equal starts mean identical buffers, which
+// the kernels allow (each element is read before it is written, by the thread
+// that writes it, or -- for LL -- before its flag is published).
+bool overlapping(const void* const* send, void* const* recv, int P, size_t bytes) {
+  std::vector<uintptr_t> starts;
+  starts.reserve(2 * (size_t)P);
+  for (int r = 0; r < P; ++r) {
+    starts.push_back((uintptr_t)send[r]);
+    starts.push_back((uintptr_t)recv[r]);
+  }
+  std::sort(starts.begin(), starts.end());
+  for (size_t i = 1; i < starts.size(); ++i)
+    if (starts[i] != starts[i - 1] && starts[i] - starts[i - 1] < bytes) return true;
+  return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ar_get_error_string(ar_status_t s) {
+  switch (s) {
+    case AR_SUCCESS: return "success";
+    case AR_ERR_INVALID_ARG: return "invalid argument";
+    case AR_ERR_CUDA: return "CUDA runtime error";
+    case AR_ERR_UNSUPPORTED: return "unsupported argument combination";
+    case AR_ERR_TIMEOUT: return "LL flag wait timed out";
+    case AR_ERR_OOM: return "out of device memory";
+    default: return "unknown status";
+  }
+}
+
+ar_status_t ar_init(int nranks, ar_comm_t* out) {
+  if (!out) return AR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (nranks < 1 || nranks > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+  ar_comm* c = new (std::nothrow) ar_comm();
+  if (!c) return AR_ERR_OOM;
+  c->P = nranks;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return AR_ERR_CUDA;
+  }
+  long long ll = env_ll("AR_LL_MAX_BYTES", (long long)kDefaultLLBytes);
+  if (ll < 16) ll = 16;
+  if (ll > (long long)kMaxLLBytes) ll = (long long)kMaxLLBytes;
+  c->ll_capacity_bytes = (size_t)ll;
+  c->ll_max_bytes = (size_t)ll;
+  long long spin = env_ll("AR_LL_SPIN_LIMIT", (long long)kDefaultSpinLimit);
+  c->spin_limit = (uint32_t)std::min<long long>(std::max<long long>(spin, 1), 0xffffffffll);
+  c->debug = (int)env_ll("AR_DEBUG", 0);
+
+  c->stage_stride = (c->ll_capacity_bytes + 3) / 4 + 4;
+  const size_t stage_bytes = (size_t)nranks * c->stage_stride * sizeof(unsigned long long);
+  std::vector<int16_t> prog;
+  for (int t = 0; t < 2; ++t) emit_tree(ar::tree_root(nranks), nranks, t, prog);
+  c->prog_len = (int)prog.size() / 2;
+  if (program_depth(prog) > 16) {  // cannot happen for nranks <= AR_MAX_RANKS
+    delete c;
+    return AR_ERR_INVALID_ARG;
+  }
+  cudaError_t e = cudaMalloc(&c->staging, stage_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&c->status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&c->tree_prog, prog.size() * sizeof(int16_t));
+  if (e == cudaSuccess) e = cudaMemset(c->staging, 0, stage_bytes);
+  if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(int));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(c->tree_prog, prog.data(), prog.size() * sizeof(int16_t), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    release(c);
+    return e == cudaErrorMemoryAllocation ? AR_ERR_OOM : AR_ERR_CUDA;
+  }
+  *out = c;
+  return AR_SUCCESS;
+}
+
+ar_status_t ar_destroy(ar_comm_t c) {
+  if (!c) return AR_SUCCESS;
+  cudaError_t e = cudaDeviceSynchronize();
+  release(c);
+  return e == cudaSuccess ? AR_SUCCESS : AR_ERR_CUDA;
+}
+
+ar_status_t ar_get_status(ar_comm_t c) {
+  if (!c) return AR_ERR_INVALID_ARG;
+  int h = 0;
+  if (cudaMemcpy(&h, c->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  return (ar_status_t)h;
+}
+
+ar_status_t ar_select_algo(ar_comm_t c, size_t count, ar_dtype_t dtype, ar_algo_t algo,
+                           ar_algo_t* chosen) {
+  if (!c || !chosen || !valid_dtype(dtype) || !valid_algo(algo)) return AR_ERR_INVALID_ARG;
+  *chosen = resolve(c, count, dtype, algo);
+  return AR_SUCCESS;
+}
+
+ar_status_t ar_set_option(ar_comm_t c, ar_option_t option, long long value) {
+  if (!c) return AR_ERR_INVALID_ARG;
+  switch (option) {
+    case AR_OPT_LL_MAX_BYTES:
+      if (value < 16 || (size_t)value > c->ll_capacity_bytes) return AR_ERR_INVALID_ARG;
+      c->ll_max_bytes = (size_t)value;
+      return AR_SUCCESS;
+    case AR_OPT_LL_SPIN_LIMIT:
+      if (value < 1 || value > 0xffffffffll) return AR_ERR_INVALID_ARG;
+      c->spin_limit = (uint32_t)value;
+      return AR_SUCCESS;
+    case AR_OPT_DEBUG:
+      c->debug = value != 0;
+      return AR_SUCCESS;
+    case AR_OPT_LL_SKIP_PRODUCER:
+      c->skip_produce = value != 0;
+      return AR_SUCCESS;
+    default:
+      return AR_ERR_INVALID_ARG;
+  }
+}
+
+ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* recvbufs,
+                         size_t count, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo, float scale,
+                         void* stream) {
+  if (!c || !valid_dtype(dtype) || !valid_op(op) || !valid_algo(algo)) return AR_ERR_INVALID_ARG;
+  if (scale != 1.0f && (dtype == AR_INT32 || op != AR_SUM)) return AR_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return AR_ERR_INVALID_ARG;  // NaN scale
+  if (count == 0) return AR_SUCCESS;
+  if (!sendbufs || !recvbufs) return AR_ERR_INVALID_ARG;
+  const size_t esize = ar::elem_bytes(dtype);
+  if (count > ((size_t)1 << 62) / esize) return AR_ERR_INVALID_ARG;
+  const int P = c->P;
+  for (int r = 0; r < P; ++r) {
+    if (!sendbufs[r] || !recvbufs[r]) return AR_ERR_INVALID_ARG;
+    if (((uintptr_t)sendbufs[r] | (uintptr_t)recvbufs[r]) & 15u) return AR_ERR_INVALID_ARG;
+  }
+  if (overlapping(sendbufs, recvbufs, P, count * esize)) return AR_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  if (dev != c->device) return AR_ERR_INVALID_ARG;
+
+  const ar_algo_t chosen = resolve(c, count, dtype, algo);
+  if (chosen == AR_ALGO_LL && count * esize > c->ll_max_bytes) return AR_ERR_UNSUPPORTED;
+
+  ar::Call call;
+  call.P = P;
+  call.send = sendbufs;
+  call.recv = recvbufs;
+  call.count = count;
+  call.dtype = dtype;
+  call.op = op;
+  call.algo = chosen == AR_ALGO_TREE ? ar::kTree : ar::kRing;
+  call.scale = scale;
+  call.stream = static_cast<cudaStream_t>(stream);
+  call.sms = c->sms;
+  call.tree_prog = c->tree_prog;
+  call.prog_len = c->prog_len;
+  call.staging = c->staging;
+  call.stage_stride = c->stage_stride;
+  call.status = c->status;
+  call.spin_limit = c->spin_limit;
+  call.skip_produce = c->skip_produce;
+  call.epoch = 0;
+
+  ar::LaunchInfo info;
+  cudaError_t e;
+  if (chosen == AR_ALGO_LL) {
+    if (c->epoch == 0xffffffffu) {
+      // every flag value has been used once: clear the staging and restart
+      e = cudaMemsetAsync(c->staging, 0, (size_t)P * c->stage_stride * sizeof(unsigned long long),
+                          call.stream);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+      }
+      c->epoch = 0;
+    }
+    call.epoch = ++c->epoch;
+    e = ar::launch_ll(call, &info);
+  } else if (P <= ar::kMaxStaticRanks) {
+    e = dtype == AR_FLOAT32    ? ar::launch_static_f32(call, &info)
+        : dtype == AR_BFLOAT16 ? ar::launch_static_bf16(call, &info)
+                               : ar::launch_static_i32(call, &info);
+  } else {
+    e = ar::launch_generic(call, &info);
+  }
+  if (c->debug) {
+    std::fprintf(stderr,
+                 "[ar] P=%d count=%zu dtype=%s op=%s algo=%s->%s kernel=%s grid=%d block=%d "
+                 "smem=%zu bytes/rank=%zu epoch=%u status=%s\n",
+                 P, count, dtype_name(dtype), op_name(op), algo_name(algo), algo_name(chosen),
+                 info.kernel, info.grid, info.block, info.smem, count * esize, call.epoch,
+                 cudaGetErrorString(e));
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  return AR_SUCCESS;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// ar_launch.h -- internal interface between the C ABI (ar_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ar {
+
+// Ranks up to this count run a kernel specialised on the exact rank count
+// (all P input vectors held in registers); larger P runs the staged kernel.
+constexpr int kMaxStaticRanks = 8;
+
+// One all-reduce call as the kernels see it.
+struct Call {
+  int P;
+  const void* const* send;  // host array of P device pointers
+  void* const* recv;        // host array of P device pointers
+  size_t count;             // elements per rank
+  int dtype, op, algo;      // ar_dtype_t, ar_op_t, resolved ar_algo_t (never AUTO)
+  float scale;
+  cudaStream_t stream;
+  int sms;                  // multiprocessors of the device
+  // TREE for P > kMaxStaticRanks: postorder programs of tree 0 and tree 1
+  // (device memory, 2 * prog_len entries; >= 0 push that rank, -1 combine).
+  const int16_t* tree_prog;
+  int prog_len;
+  // LL protocol state
+  unsigned long long* staging;  // P slots of stage_stride 8-byte words
+  size_t stage_stride;
+  int* status;                  // device status word (ar_status_t)
+  uint32_t epoch;
+  uint32_t spin_limit;
+  int skip_produce;
+};
+
+// What was launched, for AR_DEBUG logging.
+struct LaunchInfo {
+  const char* kernel = "";
+  int grid = 0;
+  int block = 0;
+  size_t smem = 0;
+};
+
+// Elements per 16-byte vector.
+inline int vec_elems(int dtype) { return dtype == 1 ? 8 : 4; }
+inline size_t elem_bytes(int dtype) { return dtype == 1 ? 2 : 4; }
+
+cudaError_t launch_static_f32(const Call& c, LaunchInfo* info);
+cudaError_t launch_static_bf16(const Call& c, LaunchInfo* info);
+cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
+cudaError_t launch_generic(const Call& c, LaunchInfo* info);
+cudaError_t launch_ll(const Call& c, LaunchInfo* info);
+
+// Ring chunk length in vectors and first vector of tree 1, for `count`.
+inline uint64_t ring_chunk_vectors(size_t count, int P, int dtype) {
+  const uint64_t V = (uint64_t)vec_elems(dtype);
+  const uint64_t per = (count + (uint64_t)P - 1) / (uint64_t)P;
+  return (per + V - 1) / V;
+}
+inline uint64_t tree_split_vectors(size_t count, int dtype) {
+  const uint64_t V = (uint64_t)vec_elems(dtype);
+  uint64_t h = ((count + 1) / 2 + V - 1) / V * V;
+  if (h > count) h = count;
+  return (h + V - 1) / V;
+}
+
+}  // namespace ar

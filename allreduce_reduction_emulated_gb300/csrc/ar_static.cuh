@@ -1,0 +1,177 @@
+// ar_static.cuh -- ring-order and tree-order all-reduce kernels specialised
+// on the exact rank count NP (1..8).
+//
+// One fused pass: each thread loads one 16-byte vector from each of the NP
+// send buffers, folds the NP vectors in registers in the algorithm's order
+// (the ring's rotation or the tree's nested expression, both resolved at
+// compile time), applies the scale / narrowing epilogue once and stores the
+// result vector to all NP receive buffers.  The ring and tree "steps" are a
+// combination order here, not data movement: every input byte is read once
+// and every output byte written once, the minimum 2 * NP * count * size
+// bytes of HBM traffic.
+#pragma once
+
+#include "ar_device.cuh"
+#include "ar_launch.h"
+
+namespace ar {
+
+constexpr int kStaticThreads = 256;
+constexpr int kStaticUnroll = 2;  // vectors per rank in flight per thread
+
+template <int NP>
+struct StaticParams {
+  const uint4* send[NP];
+  uint4* recv[NP];
+  uint64_t nfull;  // whole 16-byte vectors per rank
+  uint64_t split;  // ring: vectors per chunk; tree: first vector folded along tree 1
+  float scale;
+  int do_scale;
+  int tail;        // elements in the trailing partial vector (0 = none)
+};
+
+// Ring order for a vector of chunk C: x_C, then x_{C+1}, ..., x_{C+NP-1}.
+template <int NP, int DT, int OP, int C>
+__device__ __forceinline__ Acc<DT> ring_from(const uint4 (&r)[NP]) {
+  Acc<DT> acc = widen<DT>(r[C]);
+#pragma unroll
+  for (int k = 1; k < NP; ++k) fold<DT, OP>(acc, widen<DT>(r[(C + k) % NP]));
+  return acc;
+}
+
+// Selects the chunk's fold at run time; every branch has static register
+// indices, so the rotation costs no dynamic indexing.
+template <int NP, int DT, int OP, int C = 0>
+__device__ __forceinline__ Acc<DT> ring_fold(const uint4 (&r)[NP], int c) {
+  if constexpr (C == NP - 1) {
+    return ring_from<NP, DT, OP, C>(r);
+  } else {
+    if (c == C) return ring_from<NP, DT, OP, C>(r);
+    return ring_fold<NP, DT, OP, C + 1>(r, c);
+  }
+}
+
+// Tree T's value at label V: ((own (+) left) (+) right).
+template <int NP, int DT, int OP, int T, int V>
+__device__ __forceinline__ Acc<DT> tree_node(const uint4 (&r)[NP]) {
+  Acc<DT> acc = widen<DT>(r[tree_owner(V, NP, T)]);
+  constexpr int kLeft = tree_left(V);
+  constexpr int kRight = tree_right(V, NP);
+  if constexpr (kLeft != 0) fold<DT, OP>(acc, tree_node<NP, DT, OP, T, kLeft>(r));
+  if constexpr (kRight != 0) fold<DT, OP>(acc, tree_node<NP, DT, OP, T, kRight>(r));
+  return acc;
+}
+
+template <int NP, int DT, int OP, int ALGO>
+__device__ __forceinline__ Acc<DT> reduce_vec(const uint4 (&r)[NP], uint64_t v, uint64_t split) {
+  if constexpr (ALGO == kRing) {
+    const int c = (v < 0xffffffffull && split < 0xffffffffull) ? (int)((uint32_t)v / (uint32_t)split)
+                                                                : (int)(v / split);
+    return ring_fold<NP, DT, OP>(r, c);
+  } else {
+    if (v < split) return tree_node<NP, DT, OP, 0, tree_root(NP)>(r);
+    return tree_node<NP, DT, OP, 1, tree_root(NP)>(r);
+  }
+}
+
+template <int NP, int DT, int OP, int ALGO>
+__global__ void __launch_bounds__(kStaticThreads)
+    static_allreduce_kernel(const __grid_constant__ StaticParams<NP> p) {
+  constexpr int U = kStaticUnroll;
+  const uint64_t n = p.nfull;
+  const uint64_t step = (uint64_t)gridDim.x * (kStaticThreads * U);
+  for (uint64_t base = (uint64_t)blockIdx.x * (kStaticThreads * U) + threadIdx.x; base < n;
+       base += step) {
+    uint4 r[U][NP];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + (uint64_t)u * kStaticThreads;
+      if (v < n) {
+#pragma unroll
+        for (int k = 0; k < NP; ++k) r[u][k] = ld_stream(p.send[k] + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + (uint64_t)u * kStaticThreads;
+      if (v < n) {
+        const uint4 o =
+            narrow<DT>(reduce_vec<NP, DT, OP, ALGO>(r[u], v, p.split), p.scale, p.do_scale != 0);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) st_stream(p.recv[k] + v, o);
+      }
+    }
+  }
+  if (p.tail != 0 && blockIdx.x == 0 && threadIdx.x == 0) {
+    uint4 r[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) r[k] = load_partial<DT>(p.send[k] + n, p.tail);
+    const uint4 o =
+        narrow<DT>(reduce_vec<NP, DT, OP, ALGO>(r, n, p.split), p.scale, p.do_scale != 0);
+#pragma unroll
+    for (int k = 0; k < NP; ++k) store_partial<DT>(p.recv[k] + n, o, p.tail);
+  }
+}
+
+template <int DT, int NP, int OP, int ALGO>
+cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
+  constexpr int U = kStaticUnroll;
+  auto kernel = static_allreduce_kernel<NP, DT, OP, ALGO>;
+  StaticParams<NP> p;
+  for (int k = 0; k < NP; ++k) {
+    p.send[k] = static_cast<const uint4*>(c.send[k]);
+    p.recv[k] = static_cast<uint4*>(c.recv[k]);
+  }
+  const uint64_t V = (uint64_t)vec_elems(DT);
+  p.nfull = c.count / V;
+  p.tail = (int)(c.count % V);
+  p.split = ALGO == kRing ? ring_chunk_vectors(c.count, NP, DT) : tree_split_vectors(c.count, DT);
+  p.scale = c.scale;
+  p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
+  static const int blocks_per_sm = [&] {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kStaticThreads, 0) != cudaSuccess)
+      b = 1;
+    return b > 0 ? b : 1;
+  }();
+  const uint64_t need = (p.nfull + kStaticThreads * U - 1) / (kStaticThreads * U);
+  const uint64_t cap = (uint64_t)c.sms * (uint64_t)blocks_per_sm;
+  const int grid = (int)(need < 1 ? 1 : (need < cap ? need : cap));
+  kernel<<<grid, kStaticThreads, 0, c.stream>>>(p);
+  info->kernel = ALGO == kRing ? "static_ring" : "static_tree";
+  info->grid = grid;
+  info->block = kStaticThreads;
+  info->smem = 0;
+  return cudaGetLastError();
+}
+
+template <int DT, int NP>
+cudaError_t launch_static_np(const Call& c, LaunchInfo* info) {
+  const int key = c.op * 4 + c.algo;
+  switch (key) {
+    case kSum * 4 + kRing: return launch_static_one<DT, NP, kSum, kRing>(c, info);
+    case kSum * 4 + kTree: return launch_static_one<DT, NP, kSum, kTree>(c, info);
+    case kMin * 4 + kRing: return launch_static_one<DT, NP, kMin, kRing>(c, info);
+    case kMin * 4 + kTree: return launch_static_one<DT, NP, kMin, kTree>(c, info);
+    case kMax * 4 + kRing: return launch_static_one<DT, NP, kMax, kRing>(c, info);
+    case kMax * 4 + kTree: return launch_static_one<DT, NP, kMax, kTree>(c, info);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int DT>
+cudaError_t launch_static_dt(const Call& c, LaunchInfo* info) {
+  switch (c.P) {
+    case 1: return launch_static_np<DT, 1>(c, info);
+    case 2: return launch_static_np<DT, 2>(c, info);
+    case 3: return launch_static_np<DT, 3>(c, info);
+    case 4: return launch_static_np<DT, 4>(c, info);
+    case 5: return launch_static_np<DT, 5>(c, info);
+    case 6: return launch_static_np<DT, 6>(c, info);
+    case 7: return launch_static_np<DT, 7>(c, info);
+    case 8: return launch_static_np<DT, 8>(c, info);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ar

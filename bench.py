@@ -1,0 +1,409 @@
+#!/usr/bin/env python3
+"""Throughput of the emulated all-reduce on GB300.
+
+One step = one all-reduce call over the workload (P emulated ranks' buffers
+resident in HBM).  Default workload: P = 8 ranks x 16,777,216 fp32 (64 MiB per
+rank) of N(0, 1e-3) gradients from seed 0, sum in ring order with the fused
+1/8 DDP-mean scale.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  value = algbw (bytes per rank / time, summed over the N
+replicas); busbw = algbw * 2(P-1)/P; roofline.frac = (2 * P * count * size / t)
+/ measured HBM copy bandwidth.  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU (the emulated all-reduce never talks
+between GPUs); timing takes the max over ranks.  --impl reference times the
+CPU oracle on host cores on a bounded slice of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "allreduce algbw/busbw GB/s (P emulated ranks, 1 GB300) and % of HBM roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["allreduce_reduction_emulated_gb300/csrc/ar_device.cuh",
+                  "allreduce_reduction_emulated_gb300/csrc/ar_static.cuh",
+                  "allreduce_reduction_emulated_gb300/csrc/ar_static_f32.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "static_ring_p8_64MiB_fp32.ncu.txt")
+
+WORKLOADS = {
+    # the headline: 8 ranks x 64 MiB fp32, ring order, DDP mean
+    "p8_64MiB_fp32_ring_ddp_mean": dict(P=8, count=16 * 1024 * 1024, kind="normal", sigma=1e-3,
+                                        dtype="f32", op="sum", algo="ring", scale=0.125, seed=0),
+    # other sizes for exploration (parity cases, not the headline line)
+    "p8_256MiB_bf16_tree": dict(P=8, count=128 * 1024 * 1024, kind="normal_bf16", sigma=1e-2,
+                                dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
+    "p72_16MiB_int32_sum_ring": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
+                                     dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
+    "p8_4KiB_fp32_ll": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
+                            algo="ll", scale=1.0, seed=0),
+}
+ESIZE = {"f32": 4, "bf16": 2, "i32": 4}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="p8_64MiB_fp32_ring_ddp_mean")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def config_of(name: str, w: dict, n: int) -> dict:
+    return {"workload": name, "P": w["P"], "count_per_rank": w["count"], "dtype": w["dtype"],
+            "op": w["op"], "algo": w["algo"], "scale": w["scale"],
+            "values": f"{w['kind']} sigma={w['sigma']} seed={w['seed']}",
+            "l2": "inputs larger than L2 (no flush)" if 2 * w["P"] * w["count"] * ESIZE[w["dtype"]] > 2 * 129e6
+                  else "L2 not flushed (small message: latency-bound)",
+            "parallelism": f"replicas x{n}"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [f.strip() for f in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        rows = inside or [r for _, r in self.rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- roofline
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if key in d and d[key]:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources are unchanged since that capture."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def oracle_throughput(w: dict, host_sends, seconds: float):
+    """The oracle as it stands, one host core, over whole-workload passes."""
+    import numpy as np
+
+    import oracle
+
+    P, count = w["P"], w["count"]
+    dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
+    op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
+    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL}[w["algo"]]
+    recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
+    oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, min(count, 65536), recvs)  # warm
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, count, recvs)
+        done += count
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 8 * count:
+            break
+    return done * ESIZE[w["dtype"]] / el / 1e9, done // count, el
+
+
+def reference_arm(args, w, name):
+    """--impl reference: the CPU oracle on a bounded slice of the workload."""
+    import numpy as np
+
+    import oracle
+    import synthetic
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    P, count = w["P"], w["count"]
+    dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
+    op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
+    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL}[w["algo"]]
+    # calibrate, then size the per-step slice so that warmup + steps take ~60 s
+    probe = min(count, 32768)
+    idx = np.arange(probe)
+    sends = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
+    for r in range(P):
+        sends[r][:probe] = synthetic.values_np(w["kind"], w["seed"], r, idx, w["sigma"])
+    recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
+    t0 = time.perf_counter()
+    oracle.allreduce(sends, dt, op, algo, w["scale"], 0, probe, recvs)
+    per_elem = max((time.perf_counter() - t0) / probe, 1e-9)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    S = int(min(count, max(1024, budget / per_elem)))
+    S = max(1, S // 1024 * 1024) if S >= 1024 else S
+    if S > probe:
+        idx = np.arange(probe, S)
+        for r in range(P):
+            sends[r][probe:S] = synthetic.values_np(w["kind"], w["seed"], r, idx, w["sigma"])
+    for _ in range(args.warmup):
+        oracle.allreduce(sends, dt, op, algo, w["scale"], 0, S, recvs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.allreduce(sends, dt, op, algo, w["scale"], 0, S, recvs)
+    el = time.perf_counter() - t0
+    value = S * ESIZE[w["dtype"]] * args.steps / el / 1e9
+    sample = (f"elements [0, {S}) of each of the {P} ranks' {count}-element buffers per step "
+              f"(ring chunking of the full count), one host core")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
+        "data": "synthetic", "config": config_of(name, w, args.gpus),
+        "busbw": value * 2 * (P - 1) / P,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- our arm
+
+def ours_arm(args, w, name):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import allreduce_reduction_emulated_gb300 as ar
+    import synthetic
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    P, count = w["P"], w["count"]
+    esize = ESIZE[w["dtype"]]
+    dtype = {"f32": ar.AR_FLOAT32, "bf16": ar.AR_BFLOAT16, "i32": ar.AR_INT32}[w["dtype"]]
+    op = ar.OPS[w["op"]]
+    algo = ar.ALGOS[w["algo"]]
+    sends = [synthetic.values_torch(w["kind"], w["seed"], r, 0, count, dev, w["sigma"]) for r in range(P)]
+    recvs = [torch.empty_like(s) for s in sends]
+    comm = ar.ar_init(P)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ar.ar_allreduce(comm, sends, recvs, count, dtype, op, algo, w["scale"], stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+        raise SystemExit("device status error in warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    time.sleep(0.2)
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+        raise SystemExit("device status error in the timed region")
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    algbw = world * count * esize / (ms_step * 1e-3) / 1e9
+    hbm_bytes = 2 * P * count * esize
+    achieved = hbm_bytes / (ms_step * 1e-3) / 1e9           # one kernel per step
+    peak, peak_kind = measured_hbm_peak()
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the all-reduce, D2H of every rank's result
+    host_in = [s.cpu().pin_memory() for s in sends]
+    host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+
+    def e2e_step():
+        for d, h in zip(sends, host_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(host_out, recvs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * count * esize / (e2e_ms * 1e-3) / 1e9
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1:
+            host_np = [h.numpy() if h.dtype != torch.bfloat16 else h.view(torch.int16).numpy().view(np.uint16)
+                       for h in host_in]
+            gbs, passes, el = oracle_throughput(w, host_np, args.cpu_seconds)
+            cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{passes} full pass(es) over the workload ({P} x {count} elements), "
+                             f"{el:.1f} s on one host core"}
+        traffic = profiled_traffic()
+        line = {
+            "metric": METRIC, "value": algbw, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+            "config": config_of(name, w, world),
+            "busbw": algbw * 2 * (P - 1) / P,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": hbm_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": P * count * esize, "d2h_bytes_per_step": P * count * esize},
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(t0, t1),
+        }
+        print(json.dumps(line), flush=True)
+    ar.ar_destroy(comm)
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w, args.workload)
+    else:
+        ours_arm(args, w, args.workload)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * ar.h -- C ABI of libar.so: an all-reduce over P ranks emulated as P separate
+ * buffers in one GPU's memory.
+ *
+ * The operation ("NCCL, NIXL, and Distributed GPU Communication", section
+ * "All-reduce"): every rank's buffer is reduced elementwise with sum, min or
+ * max, and the single result is stored in every rank's receive buffer; DDP
+ * then divides it by world_size (the fused `scale` below).  The call mirrors
+ * the pages' host-side NCCL pattern ("NCCL and NVSHMEM -- two GPU communication
+ * models, side by side", host-code example: ncclCommInitRank once, then
+ * ncclAllReduce(sendbuff, recvbuff, count, datatype, op, comm, stream), then
+ * cudaStreamSynchronize).  Because one process holds all P emulated ranks, the
+ * rank id disappears and send / receive buffers become arrays of P pointers.
+ *
+ * Combination order (which partial sums are formed) is part of the result for
+ * floating-point data:
+ *   AR_ALGO_RING -- reduce-scatter of P chunks followed by all-gather ("NCCL,
+ *     NIXL, ...", section "Reduce-scatter": all-reduce = reduce-scatter +
+ *     all-gather; lecture_068 page, section 05: the ring takes 2(N-1) steps).
+ *     The count is cut into P chunks of L = roundup(ceil(count/P), V) elements,
+ *     V = 16 / sizeof(element); element e of chunk c is folded as
+ *     x_c, then (+) x_{c+1}, ..., (+) x_{c+P-1} (ranks mod P).
+ *   AR_ALGO_TREE -- the double binary tree ("NCCL and NVSHMEM ...", section
+ *     "double binary tree": two complementary binary trees at once).  Labels
+ *     1..P form an in-order binary tree rooted at the largest power of two <= P
+ *     (label v with lowbit b >= 2 has children v - b/2 and v + h, h the largest
+ *     of b/2, b/4, ..., 1 with v + h <= P).  Tree 0 puts rank r at label r+1,
+ *     tree 1 puts it one label earlier (label v -> rank v mod P).  A node's
+ *     value is ((own (+) left) (+) right).  Elements [0, H) follow tree 0 and
+ *     [H, count) tree 1, H = min(count, roundup(ceil(count/2), V)).
+ *   AR_ALGO_LL -- the small-message protocol of "Demystifying NVSHMEM" (the
+ *     collectives paragraph: LL packs data and its arrival flag into one
+ *     atomic write): each rank's 4-byte payload words are staged as 8-byte
+ *     {payload, flag = per-call epoch} words, reducers poll the flags (bounded
+ *     spin) and fold in the RING order, so LL == RING bit for bit.
+ *   AR_ALGO_AUTO -- LL when count * sizeof(element) <= the LL limit (64 KiB by
+ *     default), RING above it (NCCL picks tree for small and ring for large
+ *     messages by itself: "NCCL and NVSHMEM ...", the ring / tree paragraph).
+ * Accumulation: fp32 for fp32 and bf16 data (bf16 rounded once, to nearest
+ * even, at the end), two's-complement wrap-around for int32.  Min / max keep
+ * the earlier operand of a tie in fold order.
+ *
+ * Threading: a communicator is not thread-safe, and only one ar_allreduce may
+ * be in flight on it at a time (calls on one stream are ordered, so that is
+ * the normal case); two concurrent collectives need two communicators
+ * ("Demystifying NVSHMEM": two concurrent collectives on one PE may not share
+ * a team's internal resources).
+ */
+#ifndef AR_H_
+#define AR_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque communicator.  Created once and reused ("NCCL, NIXL, ...", checklist
+ * item "NCCL communicator ... must not be created inside the loop"). */
+typedef struct ar_comm* ar_comm_t;
+
+typedef enum {
+    AR_SUCCESS = 0,
+    AR_ERR_INVALID_ARG = 1,  /* bad pointer, alignment, overlap, size or enum value     */
+    AR_ERR_CUDA = 2,         /* a CUDA runtime call failed (no device, launch failure)   */
+    AR_ERR_UNSUPPORTED = 3,  /* valid but not provided: scale != 1 for int32 / min / max,
+                                LL above the LL limit                                    */
+    AR_ERR_TIMEOUT = 4,      /* device side: an LL flag wait hit its spin limit         */
+    AR_ERR_OOM = 5           /* ar_init could not allocate its device memory            */
+} ar_status_t;
+
+typedef enum { AR_FLOAT32 = 0, AR_BFLOAT16 = 1, AR_INT32 = 2 } ar_dtype_t;
+typedef enum { AR_SUM = 0, AR_MIN = 1, AR_MAX = 2 } ar_op_t;
+typedef enum { AR_ALGO_AUTO = 0, AR_ALGO_RING = 1, AR_ALGO_TREE = 2, AR_ALGO_LL = 3 } ar_algo_t;
+
+/* Largest number of emulated ranks one communicator takes. */
+#define AR_MAX_RANKS 256
+
+/*
+ * Creates a communicator for `nranks` emulated ranks (1 .. AR_MAX_RANKS) on
+ * the calling thread's current CUDA device and stores it in *out.  Allocates
+ * the LL staging area (nranks * LL limit * 2 bytes: 8-byte words carrying
+ * 4-byte payloads), a device status word and the tree schedules; reads the
+ * environment defaults AR_DEBUG, AR_LL_MAX_BYTES and AR_LL_SPIN_LIMIT.
+ * Synchronous.  Errors: AR_ERR_INVALID_ARG (out == NULL or nranks out of
+ * range), AR_ERR_CUDA (no usable device), AR_ERR_OOM.  On error *out is NULL.
+ */
+ar_status_t ar_init(int nranks, ar_comm_t* out);
+
+/*
+ * All-reduce of P = nranks buffers (definition and orders above).
+ *   sendbufs  host array of P device pointers; sendbufs[r] holds rank r's
+ *             `count` elements.  Read only.
+ *   recvbufs  host array of P device pointers; recvbufs[r] receives the
+ *             `count`-element result.  recvbufs[r] == sendbufs[r] (in place)
+ *             is allowed; so is any exact aliasing of two buffers.  Buffers
+ *             that overlap without starting at the same address are rejected.
+ *   count     elements per rank; 0 is a no-op returning AR_SUCCESS.
+ *   scale     multiplies the reduced value once, in fp32, before the final
+ *             rounding (1.0f = none; 1/P gives the DDP mean).  Only for
+ *             AR_SUM on AR_FLOAT32 / AR_BFLOAT16; otherwise it must be 1.0f.
+ *   stream    a cudaStream_t (NULL = legacy default stream).
+ * The caller owns every buffer; the pointer arrays are read during the call
+ * only.  Every pointer must be 16-byte aligned device memory of the
+ * communicator's device, and that device must be current.
+ * Asynchronous: returns after enqueueing one kernel on `stream` (none when
+ * count == 0).  Argument errors return synchronously (AR_ERR_INVALID_ARG,
+ * AR_ERR_UNSUPPORTED) before anything is enqueued; launch failures return
+ * AR_ERR_CUDA; device-side errors (LL spin limit) are reported later by
+ * ar_get_status.
+ */
+ar_status_t ar_allreduce(ar_comm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                         size_t count, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,
+                         float scale, void* stream);
+
+/*
+ * Device-side status of the calls made so far on `comm`: AR_SUCCESS or
+ * AR_ERR_TIMEOUT (an LL flag wait gave up; that call's output is incomplete).
+ * Reads and clears the device status word with a synchronous copy, so call it
+ * after synchronizing the streams the calls ran on.  AR_ERR_CUDA if the copy
+ * fails, AR_ERR_INVALID_ARG for a NULL comm.
+ */
+ar_status_t ar_get_status(ar_comm_t comm);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* ar_get_error_string(ar_status_t status);
+
+/* Frees the communicator's device memory.  Synchronizes the device first.
+ * NULL is accepted (no-op). */
+ar_status_t ar_destroy(ar_comm_t comm);
+
+/*
+ * Algorithm the call would run for these arguments: AR_ALGO_AUTO resolves to
+ * AR_ALGO_LL when count * sizeof(dtype) <= the LL limit, else AR_ALGO_RING;
+ * a forced algorithm is returned as is.  Host only, touches no device.
+ */
+ar_status_t ar_select_algo(ar_comm_t comm, size_t count, ar_dtype_t dtype, ar_algo_t algo,
+                           ar_algo_t* chosen);
+
+/* Per-communicator options (host only; take effect on the next call). */
+typedef enum {
+    AR_OPT_LL_MAX_BYTES = 0,     /* LL limit in bytes per rank, 16 .. the size given
+                                    at ar_init (default 65536 or AR_LL_MAX_BYTES)       */
+    AR_OPT_LL_SPIN_LIMIT = 1,    /* polls of one flag before AR_ERR_TIMEOUT (>= 1)     */
+    AR_OPT_DEBUG = 2,            /* nonzero: one line per call on stderr               */
+    AR_OPT_LL_SKIP_PRODUCER = 3  /* test hook: LL kernels skip staging, so every flag
+                                    wait runs out and reports AR_ERR_TIMEOUT           */
+} ar_option_t;
+
+ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_H_ */
