@@ -26,20 +26,42 @@ template <int DT> struct Acc {
 
 // ----------------------------------------------------------------- memory
 
+// Cache hints of the streaming accesses (compile-time tunables).
+#ifndef AR_LD_HINT
+#define AR_LD_HINT 0
+#endif
+#ifndef AR_ST_HINT
+#define AR_ST_HINT 0
+#endif
+#if AR_LD_HINT == 0
+#define AR_LD_OP "ld.global.L1::no_allocate.v4.u32"
+#elif AR_LD_HINT == 1
+#define AR_LD_OP "ld.global.nc.L1::no_allocate.v4.u32"
+#elif AR_LD_HINT == 2
+#define AR_LD_OP "ld.global.cs.v4.u32"
+#else
+#define AR_LD_OP "ld.global.L1::no_allocate.L2::256B.v4.u32"
+#endif
+#if AR_ST_HINT == 0
+#define AR_ST_OP "st.global.cs.v4.u32"
+#elif AR_ST_HINT == 1
+#define AR_ST_OP "st.global.v4.u32"
+#else
+#define AR_ST_OP "st.global.L1::no_allocate.v4.u32"
+#endif
+
 // Streaming 16-byte load: each input element is read exactly once, so it
 // is not kept in L1.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 r;
-  asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+  asm(AR_LD_OP " {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
 
-// Streaming 16-byte store (evict-first): outputs are not re-read here.
+// Streaming 16-byte store: outputs are not re-read by this kernel.
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w));
+  asm volatile(AR_ST_OP " [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w));
 }
 
 // 8-byte accesses used by the LL protocol.  A naturally aligned 64-bit access

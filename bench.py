@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="p8_64MiB_fp32_ring_ddp_mean")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="message-size sweep (P=8 fp32, 8 B .. 1 GiB per rank) with an alpha-beta fit")
     return ap.parse_args()
 
 
@@ -172,6 +174,24 @@ def profiled_traffic():
         return float(fields["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+# ------------------------------------------------------------ aggregation
+
+def max_over_ranks(x: float, dist=None) -> float:
+    """The slowest rank's time (every rank gets it)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_replica_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every replica's bytes over the slowest replica's time."""
+    return world * bytes_per_replica_step / (ms_per_step * 1e-3) / 1e9
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -306,10 +326,12 @@ def ours_arm(args, w, name):
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    torch.cuda.nvtx.range_push("timed")      # lets a profiler select exactly this region
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t1 = time.time()
     if dist:
@@ -319,46 +341,62 @@ def ours_arm(args, w, name):
     ms = ev0.elapsed_time(ev1)
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error in the timed region")
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / args.steps
-    algbw = world * count * esize / (ms_step * 1e-3) / 1e9
+    ms_step = max_over_ranks(ms, dist) / args.steps
+    algbw = job_gbs(count * esize, ms_step, world)
     hbm_bytes = 2 * P * count * esize
     achieved = hbm_bytes / (ms_step * 1e-3) / 1e9           # one kernel per step
     peak, peak_kind = measured_hbm_peak()
 
-    # end to end through the public API with host buffers: pinned H2D of the
-    # step's inputs, the all-reduce, D2H of every rank's result
+    # end to end through the public API with host buffers: every step copies
+    # its P inputs from pinned host memory, runs the call and copies all P
+    # results back.  Steps are pipelined over two device buffer sets and three
+    # streams (H2D of step i+1 and D2H of step i-1 overlap the call of step i).
     host_in = [s.cpu().pin_memory() for s in sends]
     host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+    sets = [(sends, recvs), ([torch.empty_like(s) for s in sends], [torch.empty_like(s) for s in sends])]
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    nsteps = args.e2e_steps
 
-    def e2e_step():
-        for d, h in zip(sends, host_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(host_out, recvs):
-            h.copy_(d, non_blocking=True)
+    def e2e_run(n):
+        done_run = [None] * n
+        done_out = [None] * n
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(s_in)
+        s_run.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n):
+            d_in, d_out = sets[i % 2]
+            if i >= 2:
+                s_in.wait_event(done_run[i - 2])     # step i-2 no longer reads these inputs
+            with torch.cuda.stream(s_in):
+                for d, h in zip(d_in, host_in):
+                    d.copy_(h, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(s_in)
+            s_run.wait_event(ready)
+            if i >= 2:
+                s_run.wait_event(done_out[i - 2])    # step i-2's results have left
+            ar.ar_allreduce(comm, d_in, d_out, count, dtype, op, algo, w["scale"], s_run)
+            done_run[i] = torch.cuda.Event()
+            done_run[i].record(s_run)
+            s_out.wait_event(done_run[i])
+            with torch.cuda.stream(s_out):
+                for h, d in zip(host_out, d_out):
+                    h.copy_(d, non_blocking=True)
+            done_out[i] = torch.cuda.Event()
+            done_out[i].record(s_out)
+        end.record(s_out)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
+    e2e_run(3)
     if dist:
         dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * count * esize / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_run(nsteps) / nsteps, dist)
+    if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+        raise SystemExit("device status error in the end-to-end run")
+    e2e_value = job_gbs(count * esize, e2e_ms, world)
 
     line = None
     if rank == 0:
@@ -382,8 +420,10 @@ def ours_arm(args, w, name):
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "algorithmic_bytes_per_launch": hbm_bytes},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT,
-                    "h2d_bytes_per_step": P * count * esize, "d2h_bytes_per_step": P * count * esize},
+            "e2e": {"value": e2e_value, "unit": UNIT, "steps": nsteps, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": P * count * esize, "d2h_bytes_per_step": P * count * esize,
+                    "path": "pinned host -> device copies, ar_allreduce, device -> pinned host copies "
+                            "of all P results; pipelined over 2 buffer sets / 3 streams"},
             "gpu_launches": args.steps,
             "clocks": clocks.summary(t0, t1),
         }
@@ -394,8 +434,103 @@ def ours_arm(args, w, name):
     return line
 
 
+# ------------------------------------------------------------------ sweep
+
+def fit_alpha_beta(points):
+    """Least-squares t = alpha + beta * n over (n bytes, t seconds) points."""
+    n = len(points)
+    sx = sum(p[0] for p in points)
+    sy = sum(p[1] for p in points)
+    sxx = sum(p[0] * p[0] for p in points)
+    sxy = sum(p[0] * p[1] for p in points)
+    beta = (n * sxy - sx * sy) / (n * sxx - sx * sx)
+    alpha = (sy - beta * sx) / n
+    return alpha, beta
+
+
+def sweep(args):
+    """nccl-tests style sweep ("NCCL and NVSHMEM ...", exercise 1: 8 B .. 1 GiB,
+    factor 2) for AUTO and each forced algorithm, with t = alpha + beta * n."""
+    import torch
+
+    import __graft_entry__
+    import allreduce_reduction_emulated_gb300 as ar
+    import synthetic
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    P, top = 8, 1 << 28
+    sends_full = [synthetic.values_torch("uniform", 0, r, 0, top, dev) for r in range(P)]
+    recvs_full = [torch.empty_like(s) for s in sends_full]
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    comm = ar.ar_init(P)
+    stream = torch.cuda.current_stream()
+    names = {ar.AR_ALGO_AUTO: "auto", ar.AR_ALGO_RING: "ring", ar.AR_ALGO_TREE: "tree",
+             ar.AR_ALGO_LL: "ll"}
+    rows = []
+    count = 2
+    while count <= top:
+        sends = [x[:count] for x in sends_full]
+        recvs = [x[:count] for x in recvs_full]
+        nbytes = count * 4
+        small = 2 * P * nbytes < 2 * 129e6           # working set could sit in L2: flush it
+        algos = [ar.AR_ALGO_AUTO, ar.AR_ALGO_RING, ar.AR_ALGO_TREE]
+        if nbytes <= 65536:
+            algos.append(ar.AR_ALGO_LL)
+        for algo in algos:
+            def call():
+                ar.ar_allreduce(comm, sends, recvs, count, ar.AR_FLOAT32, ar.AR_SUM, algo, 1.0, stream)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            if small:
+                times = []
+                for _ in range(50):
+                    flush.zero_()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    times.append(a.elapsed_time(b))
+                t = statistics.median(times) * 1e-3
+            else:
+                iters = max(5, min(200, int(2e9 / (2 * P * nbytes))))
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(iters):
+                    call()
+                b.record(stream)
+                torch.cuda.synchronize()
+                t = a.elapsed_time(b) * 1e-3 / iters
+            if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+                raise SystemExit("device status error in the sweep")
+            rows.append({"bytes_per_rank": nbytes, "algo": names[algo],
+                         "resolved": names[ar.ar_select_algo(comm, count, ar.AR_FLOAT32, algo)],
+                         "us": t * 1e6, "algbw": nbytes / t / 1e9,
+                         "busbw": nbytes / t / 1e9 * 2 * (P - 1) / P,
+                         "hbm_gbs": 2 * P * nbytes / t / 1e9, "l2_flushed": small})
+        count *= 2
+    ar.ar_destroy(comm)
+    fits = {}
+    for name in ("ring", "tree", "ll", "auto"):
+        pts = [(r["bytes_per_rank"], r["us"] * 1e-6) for r in rows if r["algo"] == name]
+        if len(pts) >= 2:
+            alpha, beta = fit_alpha_beta(pts)
+            fits[name] = {"alpha_us": alpha * 1e6, "inv_beta_gbs": (1 / beta / 1e9) if beta > 0 else None,
+                          "points": len(pts)}
+    print(json.dumps({"sweep": "P=8 fp32 uniform[-1,1] sum, bytes per rank 8 B .. 1 GiB (x2)",
+                      "unit": "us / GB/s", "rows": rows, "fit": fits}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        sweep(args)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
