@@ -30,6 +30,7 @@ AR_SUM, AR_MIN, AR_MAX = 0, 1, 2
 AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL = 0, 1, 2, 3
 AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER = 0, 1, 2, 3
 AR_MAX_RANKS = 256
+AR_NOALLOC_MAX_RANKS, AR_NOALLOC_MAX_BYTES = 8, 65536
 
 OPS = {"sum": AR_SUM, "min": AR_MIN, "max": AR_MAX}
 ALGOS = {"auto": AR_ALGO_AUTO, "ring": AR_ALGO_RING, "tree": AR_ALGO_TREE, "ll": AR_ALGO_LL}
@@ -71,6 +72,9 @@ def library() -> ctypes.CDLL:
                 L.ar_select_algo.restype = i
                 L.ar_set_option.argtypes = [vp, i, ctypes.c_longlong]
                 L.ar_set_option.restype = i
+                L.ar_allreduce_ll_noalloc.argtypes = [i, ctypes.POINTER(vp), ctypes.POINTER(vp), sz,
+                                                      i, i, ctypes.c_float, vp, ctypes.POINTER(i)]
+                L.ar_allreduce_ll_noalloc.restype = i
                 _lib = L
     return _lib
 
@@ -139,6 +143,28 @@ def ar_set_option(comm: int, option: int, value: int) -> None:
     st = library().ar_set_option(comm, int(option), int(value))
     if st != AR_SUCCESS:
         raise ArError(st, "ar_set_option")
+
+
+def ar_allreduce_ll_noalloc(sendbufs, recvbufs, count: int, dtype: int, op: int = AR_SUM,
+                            scale: float = 1.0, stream=None, wait_status: bool = False):
+    """LL all-reduce that allocates no device memory (for callers that cannot).
+
+    Limited to AR_NOALLOC_MAX_RANKS ranks and AR_NOALLOC_MAX_BYTES bytes per
+    rank.  With wait_status=True the call waits for the stream and returns the
+    device status (AR_SUCCESS or AR_ERR_TIMEOUT); otherwise it returns None.
+    """
+    P = len(sendbufs)
+    if len(recvbufs) != P:
+        raise ArError(AR_ERR_INVALID_ARG, "ar_allreduce_ll_noalloc: sendbufs and recvbufs differ in length")
+    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
+    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    status = ctypes.c_int(-1)
+    st = library().ar_allreduce_ll_noalloc(P, sp, rp, int(count), int(dtype), int(op), float(scale),
+                                           _stream_handle(stream),
+                                           ctypes.byref(status) if wait_status else None)
+    if st != AR_SUCCESS:
+        raise ArError(st, "ar_allreduce_ll_noalloc")
+    return status.value if wait_status else None
 
 
 # ------------------------------------------------------------- convenience

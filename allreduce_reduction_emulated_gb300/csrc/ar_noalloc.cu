@@ -1,0 +1,153 @@
+// ar_noalloc.cu -- an LL all-reduce for callers that cannot allocate device
+// memory (declared in include/ar.h as ar_allreduce_ll_noalloc).
+//
+// Some callers must not call cudaMalloc: code whose device memory is owned by a
+// framework's pool (a library allocation would bypass that pool's accounting
+// and limits), code that runs in a latency-critical loop where cudaMalloc /
+// cudaFree may synchronize the device, and code that may not allocate once it
+// has started.  A communicator (ar_init) allocates its LL staging area, so
+// this entry point instead keeps the staging area and the status word in one
+// fixed-size array compiled into the library: every GPU that loads the
+// library holds that array (about 1 MiB) until the process exits.
+//
+// The array is shared by every call on a device and keeps the last call's
+// contents.  Each call stages its words under a fresh epoch, so stale words
+// never match; when the 32-bit epoch runs out the staging words are cleared
+// once.  The status word starts at zero (module load) and is cleared whenever
+// it is read.  Calls that overlap on the GPU (for example on two streams)
+// race on the array and must not be issued.
+#include <cstdint>
+#include <mutex>
+#include <vector>
+#include <algorithm>
+
+#include "../../include/ar.h"
+#include "ar_launch.h"
+
+namespace {
+
+constexpr size_t kStride = AR_NOALLOC_MAX_BYTES / 4 + 4;  // 8-byte words per rank slot
+constexpr size_t kSlotsOffset = 32;                        // word 0 holds the status
+constexpr size_t kScratchWords = kSlotsOffset + (size_t)AR_NOALLOC_MAX_RANKS * kStride;
+constexpr uint32_t kSpinLimit = 1u << 22;                  // ~1 s of polls, then AR_ERR_TIMEOUT
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned long long g_noalloc_scratch[kScratchWords];
+
+namespace {
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t setup = cudaSuccess;
+  unsigned long long* base = nullptr;  // device address of g_noalloc_scratch
+  int sms = 0;
+  uint32_t epoch = 0;
+  std::mutex lock;
+};
+
+DeviceState g_state[kMaxDevices];
+
+// Once per device, with that device current: the array's device address.
+// (In host code the symbol names a host-side stand-in, not device memory.)
+void set_up(DeviceState& s, int dev) {
+  s.setup = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.base), g_noalloc_scratch);
+  if (s.setup == cudaSuccess)
+    s.setup = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+bool bad_overlap(const void* const* send, void* const* recv, int P, size_t bytes) {
+  std::vector<uintptr_t> starts;
+  for (int r = 0; r < P; ++r) {
+    starts.push_back((uintptr_t)send[r]);
+    starts.push_back((uintptr_t)recv[r]);
+  }
+  std::sort(starts.begin(), starts.end());
+  for (size_t i = 1; i < starts.size(); ++i)
+    if (starts[i] != starts[i - 1] && starts[i] - starts[i - 1] < bytes) return true;
+  return false;
+}
+
+}  // namespace
+
+extern "C" ar_status_t ar_allreduce_ll_noalloc(int nranks, const void* const* sendbufs,
+                                               void* const* recvbufs, size_t count, ar_dtype_t dtype,
+                                               ar_op_t op, float scale, void* stream,
+                                               int* device_status) {
+  if (nranks < 1) return AR_ERR_INVALID_ARG;
+  if (dtype != AR_FLOAT32 && dtype != AR_BFLOAT16 && dtype != AR_INT32) return AR_ERR_INVALID_ARG;
+  if (op != AR_SUM && op != AR_MIN && op != AR_MAX) return AR_ERR_INVALID_ARG;
+  if (!(scale == scale)) return AR_ERR_INVALID_ARG;
+  if (scale != 1.0f && (dtype == AR_INT32 || op != AR_SUM)) return AR_ERR_UNSUPPORTED;
+  const size_t esize = ar::elem_bytes(dtype);
+  // beyond the fixed array: too many ranks or too many bytes per rank
+  if (nranks > AR_NOALLOC_MAX_RANKS || count > AR_NOALLOC_MAX_BYTES / esize) return AR_ERR_UNSUPPORTED;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return AR_ERR_UNSUPPORTED;
+  DeviceState& s = g_state[dev];
+  std::call_once(s.once, set_up, std::ref(s), dev);
+  if (s.setup != cudaSuccess) return AR_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (count > 0) {
+    if (!sendbufs || !recvbufs) return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < nranks; ++r) {
+      if (!sendbufs[r] || !recvbufs[r]) return AR_ERR_INVALID_ARG;
+      if (((uintptr_t)sendbufs[r] | (uintptr_t)recvbufs[r]) & 15u) return AR_ERR_INVALID_ARG;
+    }
+    if (bad_overlap(sendbufs, recvbufs, nranks, count * esize)) return AR_ERR_INVALID_ARG;
+
+    ar::Call c;
+    c.P = nranks;
+    c.send = sendbufs;
+    c.recv = recvbufs;
+    c.count = count;
+    c.dtype = dtype;
+    c.op = op;
+    c.algo = 1;  // the ring order, which the LL protocol follows
+    c.scale = scale;
+    c.stream = st;
+    c.sms = s.sms;
+    c.tree_prog = nullptr;
+    c.prog_len = 0;
+    c.staging = s.base + kSlotsOffset;
+    c.stage_stride = kStride;
+    c.status = reinterpret_cast<int*>(s.base);
+    c.spin_limit = kSpinLimit;
+    c.skip_produce = 0;
+    cudaError_t e = cudaSuccess;
+    {
+      std::lock_guard<std::mutex> g(s.lock);
+      if (s.epoch == 0xffffffffu) {
+        // every flag value has been used: clear the staging words once
+        e = cudaMemsetAsync(c.staging, 0, (size_t)AR_NOALLOC_MAX_RANKS * kStride * 8, st);
+        s.epoch = 0;
+      }
+      c.epoch = ++s.epoch;
+    }
+    ar::LaunchInfo info;
+    if (e == cudaSuccess) e = ar::launch_ll(c, &info);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return AR_ERR_CUDA;
+    }
+  }
+
+  if (device_status) {
+    // optional, synchronous: wait for the stream, then read and clear the status word
+    int h = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess ||
+        cudaMemcpy(&h, s.base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(s.base, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return AR_ERR_CUDA;
+    }
+    *device_status = h;
+  }
+  return AR_SUCCESS;
+}

@@ -149,6 +149,44 @@ typedef enum {
 
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
 
+/*
+ * LL all-reduce that allocates nothing.  (The pages have no counterpart: this
+ * entry point exists for callers of this library that cannot allocate device
+ * memory -- code whose device memory belongs to a framework's pool, code in a
+ * latency-critical loop where cudaMalloc / cudaFree may synchronize the
+ * device, code that may not allocate after start-up -- and so cannot hold a
+ * communicator, whose ar_init allocates the LL staging area.)
+ *
+ * Same result as ar_allreduce(..., AR_ALGO_LL, ...) on the same arguments (the
+ * ring combination order).  The staging area and the status word live in one
+ * fixed array compiled into libar.so (about 1 MiB per GPU that loads the
+ * library, held until the process exits), so it serves at most
+ * AR_NOALLOC_MAX_RANKS ranks and AR_NOALLOC_MAX_BYTES bytes per rank; larger
+ * requests return AR_ERR_UNSUPPORTED.  No cudaMalloc, cudaFree or allocating
+ * library call is made.
+ *   nranks        1 .. AR_NOALLOC_MAX_RANKS emulated ranks
+ *   sendbufs,     host arrays of nranks device pointers, as for ar_allreduce
+ *   recvbufs      (16-byte aligned, no partial overlap; exact aliasing allowed)
+ *   count, dtype, op, scale, stream   as for ar_allreduce
+ *   device_status NULL: asynchronous, returns after enqueueing the kernel.
+ *                 Non-NULL: waits for `stream`, then stores AR_SUCCESS or
+ *                 AR_ERR_TIMEOUT (a flag wait ran out in this or an earlier
+ *                 call on this device) and clears the device status word.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before capturing any stream.  Every call
+ * on a device shares the one array: calls that overlap on the GPU (for example
+ * on two streams at once) race and must not be issued.
+ * Errors: AR_ERR_INVALID_ARG (bad pointer, alignment, overlap, enum, NaN
+ * scale), AR_ERR_UNSUPPORTED (limits above, scale on int32 / min / max),
+ * AR_ERR_CUDA (launch or status read failed).
+ */
+#define AR_NOALLOC_MAX_RANKS 8
+#define AR_NOALLOC_MAX_BYTES 65536
+
+ar_status_t ar_allreduce_ll_noalloc(int nranks, const void* const* sendbufs, void* const* recvbufs,
+                                    size_t count, ar_dtype_t dtype, ar_op_t op, float scale,
+                                    void* stream, int* device_status);
+
 #ifdef __cplusplus
 }
 #endif
