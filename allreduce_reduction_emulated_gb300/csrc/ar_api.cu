@@ -244,8 +244,23 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   }
   if (dev != c->device) return AR_ERR_INVALID_ARG;
 
-  const ar_algo_t chosen = resolve(c, count, dtype, algo);
+  ar_algo_t chosen = resolve(c, count, dtype, algo);
   if (chosen == AR_ALGO_LL && count * esize > c->ll_max_bytes) return AR_ERR_UNSUPPORTED;
+  if (chosen == AR_ALGO_LL) {
+    // The LL epoch is a launch parameter: a captured launch would replay one
+    // epoch forever and could accept a previous replay's staged words.  Under
+    // capture AUTO takes the ring (the same result bit for bit: LL folds in
+    // the ring order) and a forced LL is refused.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess) {
+      cudaGetLastError();
+      return AR_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) {
+      if (algo != AR_ALGO_AUTO) return AR_ERR_UNSUPPORTED;
+      chosen = AR_ALGO_RING;
+    }
+  }
 
   ar::Call call;
   call.P = P;

@@ -33,10 +33,18 @@ sys.path.insert(0, ROOT)
 METRIC = "allreduce algbw/busbw GB/s (P emulated ranks, 1 GB300) and % of HBM roofline"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["allreduce_reduction_emulated_gb300/csrc/ar_device.cuh",
-                  "allreduce_reduction_emulated_gb300/csrc/ar_static.cuh",
-                  "allreduce_reduction_emulated_gb300/csrc/ar_static_f32.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "static_ring_p8_64MiB_fp32.ncu.txt")
+_CSRC = "allreduce_reduction_emulated_gb300/csrc/"
+_STATIC = [_CSRC + "ar_device.cuh", _CSRC + "ar_static.cuh"]
+# per workload: (ncu summary under profiles/, kernel sources it was taken on,
+#                launches of the profiled case per launch of this workload)
+PROFILES = {
+    "p8_64MiB_fp32_ring_ddp_mean": ("static_ring_p8_64MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
+    "p8_64MiB_bf16_tree": ("static_tree_p8_64MiB_bf16.ncu.txt", _STATIC + [_CSRC + "ar_static_bf16.cu"], 1.0),
+    "p8_256MiB_bf16_tree": ("static_tree_p8_64MiB_bf16.ncu.txt", _STATIC + [_CSRC + "ar_static_bf16.cu"], 4.0),
+    "p72_4MiB_int32_sum_ring": ("staged_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_16MiB_int32_sum_ring": ("staged_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
+    "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll.cu"], 1.0),
+}
 
 WORKLOADS = {
     # the headline: 8 ranks x 64 MiB fp32, ring order, DDP mean
@@ -47,10 +55,21 @@ WORKLOADS = {
                                 dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
     "p72_16MiB_int32_sum_ring": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
                                      dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
+    # smaller cases of the same kernels, sized for profiler captures (inputs still exceed L2)
+    "p8_64MiB_bf16_tree": dict(P=8, count=32 * 1024 * 1024, kind="normal_bf16", sigma=1e-2,
+                               dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
+    "p72_4MiB_int32_sum_ring": dict(P=72, count=1024 * 1024, kind="int", sigma=1.0,
+                                    dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
     "p8_4KiB_fp32_ll": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
                             algo="ll", scale=1.0, seed=0),
 }
 ESIZE = {"f32": 4, "bf16": 2, "i32": 4}
+
+# DDP-style bucketed run: 24 layers of [2048x8192], [8192x2048], [2048x6144],
+# [2048x2048] fp32 gradients (1,207,959,552 per rank), flattened and cut into
+# 25 MiB buckets (184 x 6,553,600 + 1 x 2,097,152), one all-reduce per bucket.
+DDP_PARAMS = 24 * (2048 * 8192 + 8192 * 2048 + 2048 * 6144 + 2048 * 2048)
+DDP_BUCKET = 25 * 1024 * 1024 // 4
 
 
 def parse_args():
@@ -62,6 +81,8 @@ def parse_args():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="p8_64MiB_fp32_ring_ddp_mean")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ddp-buckets", action="store_true",
+                    help="DDP-style run: P=8 x 1,207,959,552 fp32 gradients in 185 x 25 MiB buckets per step")
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep (P=8 fp32, 8 B .. 1 GiB per rank) with an alpha-beta fit")
     return ap.parse_args()
@@ -151,27 +172,31 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    sources are unchanged since that capture."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload's
+    kernel (scaled by units processed when a smaller case was captured), or
+    None when there is none or the kernel sources changed since the capture."""
+    if workload not in PROFILES:
+        return None
+    name, sources, scale = PROFILES[workload]
     try:
         fields = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             for line in f:
                 if ":" in line:
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        if fields.get("source_sha256") != kernel_source_hash():
+        if fields.get("source_sha256") != kernel_source_hash(sources):
             return None
-        return float(fields["dram_bytes_per_launch"])
+        return float(fields["dram_bytes_per_launch"]) * scale
     except (OSError, KeyError, ValueError):
         return None
 
@@ -408,7 +433,7 @@ def ours_arm(args, w, name):
             cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{passes} full pass(es) over the workload ({P} x {count} elements), "
                              f"{el:.1f} s on one host core"}
-        traffic = profiled_traffic()
+        traffic = profiled_traffic(name)
         line = {
             "metric": METRIC, "value": algbw, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -526,8 +551,113 @@ def sweep(args):
                       "unit": "us / GB/s", "rows": rows, "fit": fits}), flush=True)
 
 
+# ------------------------------------------------------------ DDP buckets
+
+def ddp_buckets(args):
+    """One step = the 185 bucket all-reduces of the 1.2B-parameter gradients
+    (sum, scale 1/8, ring), issued eagerly and replayed from a CUDA graph."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import allreduce_reduction_emulated_gb300 as ar
+    import oracle
+    import synthetic
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    P, total, B, sigma, seed = 8, DDP_PARAMS, DDP_BUCKET, 1e-3, 5
+    buckets = [(b, min(B, total - b)) for b in range(0, total, B)]
+    sends = []
+    for r in range(P):
+        flat = torch.empty(total, dtype=torch.float32, device=dev)
+        for start, n in buckets:
+            flat[start:start + n] = synthetic.values_torch("normal", seed, r, start, n, dev, sigma)
+        sends.append(flat)
+    recvs = [torch.empty_like(x) for x in sends]
+    comm = ar.ar_init(P)
+    stream = torch.cuda.current_stream()
+    views = [([x[s:s + n] for x in sends], [y[s:s + n] for y in recvs], n) for s, n in buckets]
+
+    def step():
+        for sv, rv, n in views:
+            ar.ar_allreduce(comm, sv, rv, n, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125)
+
+    def timed(fn, k):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(k):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / k
+
+    for _ in range(args.warmup):
+        step()
+    eager_ms = timed(step, args.steps)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    for _ in range(args.warmup):
+        g.replay()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    torch.cuda.nvtx.range_push("timed")
+    graph_ms = timed(g.replay, args.steps)
+    torch.cuda.nvtx.range_pop()
+    t1 = time.time()
+    clocks.stop()
+    if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+        raise SystemExit("device status error")
+    ar.ar_destroy(comm)
+    per_rank = total * 4
+    peak, peak_kind = measured_hbm_peak()
+    achieved = 2 * P * per_rank / (graph_ms * 1e-3) / 1e9
+    # the oracle on a bounded sample: the first buckets, each its own all-reduce
+    nb_cpu, done, t_cpu = 0, 0, 0.0
+    for start, n in buckets:
+        host = [x[start:start + n].cpu().numpy() for x in sends]
+        c0 = time.perf_counter()
+        oracle.allreduce(host, oracle.F32, oracle.SUM, oracle.RING, 0.125)
+        t_cpu += time.perf_counter() - c0
+        nb_cpu += 1
+        done += n
+        if t_cpu >= args.cpu_seconds:
+            break
+    line = {
+        "metric": METRIC, "value": per_rank / (graph_ms * 1e-3) / 1e9, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "ddp_1p2b_fp32_25MiB_buckets", "P": P, "params_per_rank": total,
+                   "buckets": len(buckets), "bucket_elems": B, "op": "sum", "algo": "ring",
+                   "scale": 0.125, "values": f"normal sigma={sigma} seed={seed}",
+                   "launch": "185 calls per step replayed from one CUDA graph",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas x1"},
+        "busbw": per_rank / (graph_ms * 1e-3) / 1e9 * 2 * (P - 1) / P,
+        "eager_ms_per_step": eager_ms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "cpu_baseline": {"value": done * 4 / t_cpu / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"the first {nb_cpu} bucket all-reduces ({done} elements per rank)"},
+        "e2e": None, "gpu_launches": len(buckets) * args.steps,
+        "clocks": clocks.summary(t0, t1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.ddp_buckets:
+        ddp_buckets(args)
+        return
     if args.sweep:
         sweep(args)
         return

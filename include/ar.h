@@ -108,6 +108,10 @@ ar_status_t ar_init(int nranks, ar_comm_t* out);
  * AR_ERR_UNSUPPORTED) before anything is enqueued; launch failures return
  * AR_ERR_CUDA; device-side errors (LL spin limit) are reported later by
  * ar_get_status.
+ * CUDA graphs: RING and TREE calls may be captured and replayed (the buffers
+ * are then fixed).  LL calls are not capturable -- each call needs a fresh
+ * epoch -- so while `stream` is capturing, AUTO resolves to RING (identical
+ * result) and a forced AR_ALGO_LL returns AR_ERR_UNSUPPORTED.
  */
 ar_status_t ar_allreduce(ar_comm_t comm, const void* const* sendbufs, void* const* recvbufs,
                          size_t count, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,

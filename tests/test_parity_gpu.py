@@ -344,3 +344,49 @@ def test_p72_int32_sum_max_min(dev, comms):
             outs[algo] = recvs[0]
         assert torch.equal(outs[ar.AR_ALGO_RING], outs[ar.AR_ALGO_TREE])
         assert torch.equal(outs[ar.AR_ALGO_RING], exact[op])
+
+
+def test_bucket_loop_captured_in_a_cuda_graph(dev, comms):
+    """A DDP-style bucket loop recorded once into a CUDA graph and replayed.
+
+    Ring and tree calls replay correctly on new data written into the same
+    buffers; under capture AUTO takes the ring for a small message (LL needs
+    a fresh epoch per call) and a forced LL is refused without disturbing the
+    capture.
+    """
+    comm = comms(8)
+    sizes = [1 << 20, 3 * (1 << 18) + 5, 1000]          # two large buckets and a small one
+    algos = [ar.AR_ALGO_RING, ar.AR_ALGO_TREE, ar.AR_ALGO_AUTO]
+    sends = [[torch.empty(n, device=dev) for _ in range(8)] for n in sizes]
+    recvs = [[torch.empty(n, device=dev) for _ in range(8)] for n in sizes]
+
+    def run_all():
+        for b, n in enumerate(sizes):
+            ar.ar_allreduce(comm, sends[b], recvs[b], n, ar.AR_FLOAT32, ar.AR_SUM, algos[b], 0.125)
+
+    run_all()                                            # warm-up outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run_all()
+            with pytest.raises(ar.ArError) as e:
+                ar.ar_allreduce(comm, sends[2], recvs[2], sizes[2], ar.AR_FLOAT32, ar.AR_SUM,
+                                ar.AR_ALGO_LL, 1.0)
+            assert e.value.status == ar.AR_ERR_UNSUPPORTED
+    rng = np.random.default_rng(41)
+    for replay in range(2):
+        host = [pins.random_inputs(rng, 8, n, ar.AR_FLOAT32) for n in sizes]
+        for b in range(len(sizes)):
+            for r in range(8):
+                sends[b][r].copy_(torch.from_numpy(host[b][r]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for b, n in enumerate(sizes):
+            oalgo = oracle.TREE if algos[b] == ar.AR_ALGO_TREE else oracle.RING
+            want = oracle.allreduce(host[b], ar.AR_FLOAT32, oracle.SUM, oalgo, 0.125)
+            for r in (0, 7):
+                pins.assert_bitwise(to_host(recvs[b][r]), want[r], f"replay {replay} bucket {b} rank {r}")
+    assert ar.ar_get_status(comm) == ar.AR_SUCCESS
