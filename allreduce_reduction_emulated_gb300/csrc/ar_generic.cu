@@ -1,14 +1,18 @@
 // ar_generic.cu -- ring-order and tree-order all-reduce for any rank count up
 // to AR_MAX_RANKS (used above the rank-specialised kernels' limit).
 //
-// With many ranks the NP input vectors of one element group no longer fit in
-// registers, and the fold order needs a dynamic rank index.  So each thread
-// stages its column -- one 16-byte vector from every rank -- in shared memory
-// with asynchronous copies (all P copies in flight at once), waits for its own
-// copies only, folds from shared memory (ring: rotated start; tree: a
-// postorder program evaluated on a small stack) and stores the result to all
-// P receive buffers.  Threads never read each other's slots, so no barrier is
-// needed.
+// With many ranks the P input vectors of a column no longer fit in registers,
+// and the fold order needs a dynamic rank index.  Each thread owns one column
+// (one 16-byte vector of every rank) and streams it through a small ring of
+// shared-memory slots in exactly the order the fold consumes it: the ring's
+// rotated rank sequence, or the tree's postorder leaf sequence.  W
+// asynchronous copies are kept in flight (cp.async, one commit group per
+// copy); before each value is used the thread waits until its copy has landed
+// (wait_group W-1: all but the W-1 newest groups done), reads it, and refills
+// the slot freed one step earlier with the copy W pushes ahead.  The tree's
+// combines run on a small stack.  Shared memory per thread is (W+1) x 16
+// bytes whatever P is, so occupancy stays high at P = 72 or 256.  Threads
+// never touch each other's slots, so there is no barrier in the main loop.
 #include "../../include/ar.h"
 #include "ar_device.cuh"
 #include "ar_launch.h"
@@ -17,12 +21,23 @@ namespace ar {
 
 namespace {
 
-constexpr int kStackDepth = 16;  // >= tree height + 1 for P <= AR_MAX_RANKS
+#ifndef AR_GENERIC_WINDOW
+#define AR_GENERIC_WINDOW 16
+#endif
+#ifndef AR_GENERIC_THREADS
+#define AR_GENERIC_THREADS 128
+#endif
+
+constexpr int kWindow = AR_GENERIC_WINDOW;    // copies in flight per thread
+constexpr int kSlots = kWindow + 1;           // one spare slot between read and refill
+constexpr int kThreads = AR_GENERIC_THREADS;
+constexpr int kStackDepth = 16;               // >= tree height + 1 for P <= AR_MAX_RANKS
+constexpr int kMaxProg = 2 * AR_MAX_RANKS;    // ops of one tree program (2P - 1)
 
 struct GenericParams {
   const uint4* send[AR_MAX_RANKS];
   uint4* recv[AR_MAX_RANKS];
-  const int16_t* prog;  // tree 0 program, then tree 1 program
+  const int16_t* prog;  // device: tree 0 program then tree 1 program (prog_len ops each)
   int prog_len;
   int P;
   uint64_t nfull;
@@ -35,31 +50,26 @@ struct GenericParams {
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
 }
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int DT, int OP, int ALGO, int T>
-__device__ __forceinline__ Acc<DT> fold_staged(const uint4* stage, int tid, const GenericParams& p,
-                                               uint64_t v) {
-  const int P = p.P;
+// Folds the column in the algorithm's order; next() yields the widened
+// input of the next rank in the push sequence.
+template <int DT, int OP, int ALGO, class Next>
+__device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ops, int nops, Next& next) {
   if constexpr (ALGO == kRing) {
-    int r = (int)(v / p.split);
-    Acc<DT> acc = widen<DT>(stage[r * T + tid]);
-    for (int k = 1; k < P; ++k) {
-      r = (r + 1 == P) ? 0 : r + 1;
-      fold<DT, OP>(acc, widen<DT>(stage[r * T + tid]));
-    }
+    Acc<DT> acc = next();
+    for (int k = 1; k < P; ++k) fold<DT, OP>(acc, next());
     return acc;
   } else {
-    const int16_t* prog = p.prog + (v < p.split ? 0 : p.prog_len);
     Acc<DT> stack[kStackDepth];
     int sp = 0;
-    for (int i = 0; i < p.prog_len; ++i) {
-      const int op = __ldg(prog + i);
-      if (op >= 0) {
-        stack[sp++] = widen<DT>(stage[op * T + tid]);
+    for (int i = 0; i < nops; ++i) {
+      if (ops[i] >= 0) {
+        stack[sp++] = next();
       } else {
         --sp;
         fold<DT, OP>(stack[sp - 1], stack[sp]);
@@ -69,31 +79,88 @@ __device__ __forceinline__ Acc<DT> fold_staged(const uint4* stage, int tid, cons
   }
 }
 
-template <int DT, int OP, int ALGO, int T>
-__global__ void __launch_bounds__(T) generic_allreduce_kernel(const __grid_constant__ GenericParams p) {
-  extern __shared__ uint4 stage[];  // [P][T]
-  const int tid = threadIdx.x;
+template <int DT, int OP, int ALGO>
+__global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __grid_constant__ GenericParams p) {
+  __shared__ uint4 slots[kSlots][kThreads];
+  __shared__ const uint4* s_send[AR_MAX_RANKS];
+  __shared__ uint4* s_recv[AR_MAX_RANKS];
+  __shared__ int16_t s_prog[2][kMaxProg];   // tree programs
+  __shared__ int16_t s_push[2][AR_MAX_RANKS];  // tree leaf (push) sequences
   const int P = p.P;
-  const uint32_t slot = (uint32_t)__cvta_generic_to_shared(stage + tid);
-  const uint64_t n = p.nfull;
-  for (uint64_t v = (uint64_t)blockIdx.x * T + tid; v < n; v += (uint64_t)gridDim.x * T) {
-    for (int r = 0; r < P; ++r) cp_async16(slot + (uint32_t)(r * T * 16), p.send[r] + v);
-    cp_async_wait_all();
-    const uint4 o =
-        narrow<DT>(fold_staged<DT, OP, ALGO, T>(stage, tid, p, v), p.scale, p.do_scale != 0);
-    for (int r = 0; r < P; ++r) st_stream(p.recv[r] + v, o);
+  const int tid = threadIdx.x;
+  for (int r = tid; r < P; r += kThreads) {
+    s_send[r] = p.send[r];
+    s_recv[r] = p.recv[r];
   }
-  if (p.tail != 0 && blockIdx.x == 0 && tid == 0) {
-    for (int r = 0; r < P; ++r) stage[r * T] = load_partial<DT>(p.send[r] + n, p.tail);
-    const uint4 o =
-        narrow<DT>(fold_staged<DT, OP, ALGO, T>(stage, 0, p, n), p.scale, p.do_scale != 0);
-    for (int r = 0; r < P; ++r) store_partial<DT>(p.recv[r] + n, o, p.tail);
+  if constexpr (ALGO == kTree) {
+    for (int t = 0; t < 2; ++t) {
+      for (int i = tid; i < p.prog_len; i += kThreads) s_prog[t][i] = p.prog[t * p.prog_len + i];
+    }
+    __syncthreads();
+    if (tid < 2) {  // leaf order = the program's pushes in order
+      int j = 0;
+      for (int i = 0; i < p.prog_len; ++i)
+        if (s_prog[tid][i] >= 0) s_push[tid][j++] = s_prog[tid][i];
+    }
+  }
+  __syncthreads();
+
+  const uint64_t v = (uint64_t)blockIdx.x * kThreads + tid;
+  const uint64_t n = p.nfull;
+  if (v > n || (v == n && p.tail == 0)) return;
+  const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
+  const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
+  const int16_t* ops = s_prog[t];
+  // rank of the k-th value in the push sequence
+  auto rank_of = [&](int k) -> int {
+    if constexpr (ALGO == kRing) {
+      int r = first + k;
+      return r >= P ? r - P : r;
+    } else {
+      return s_push[t][k];
+    }
+  };
+
+  Acc<DT> acc;
+  if (v < n) {
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(&slots[0][tid]);
+    constexpr uint32_t kSlotStride = kThreads * 16;
+#pragma unroll
+    for (int k = 0; k < kWindow; ++k) {
+      if (k < P) cp_async16(base + k * kSlotStride, s_send[rank_of(k)] + v);
+      cp_async_commit();
+    }
+    int j = 0;          // values consumed
+    int rd = 0;         // slot of value j
+    int wr = kWindow;   // slot for value j + kWindow
+    auto next = [&]() -> Acc<DT> {
+      cp_async_wait<kWindow - 1>();  // value j has landed
+      const uint4 raw = slots[rd][tid];
+      const int k = j + kWindow;
+      if (k < P) cp_async16(base + wr * kSlotStride, s_send[rank_of(k)] + v);
+      cp_async_commit();
+      ++j;
+      rd = rd + 1 == kSlots ? 0 : rd + 1;
+      wr = wr + 1 == kSlots ? 0 : wr + 1;
+      return widen<DT>(raw);
+    };
+    acc = fold_sequence<DT, OP, ALGO>(P, ops, p.prog_len, next);
+    cp_async_wait<0>();
+    const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
+    for (int r = 0; r < P; ++r) st_stream(s_recv[r] + v, o);
+  } else {
+    // the trailing partial vector: element-wise loads, same order
+    int j = 0;
+    auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[rank_of(j++)] + n, p.tail)); };
+    acc = fold_sequence<DT, OP, ALGO>(P, ops, p.prog_len, next);
+    const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
+    for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
   }
 }
 
-template <int DT, int OP, int ALGO, int T>
+template <int DT, int OP, int ALGO>
 cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
-  auto kernel = generic_allreduce_kernel<DT, OP, ALGO, T>;
+  auto kernel = generic_allreduce_kernel<DT, OP, ALGO>;
   GenericParams p;
   for (int r = 0; r < c.P; ++r) {
     p.send[r] = static_cast<const uint4*>(c.send[r]);
@@ -108,35 +175,22 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
   p.split = ALGO == kRing ? ring_chunk_vectors(c.count, c.P, DT) : tree_split_vectors(c.count, DT);
   p.scale = c.scale;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
-  const size_t smem = (size_t)c.P * T * sizeof(uint4);
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int blocks_per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, T, smem);
-  if (e != cudaSuccess) return e;
-  if (blocks_per_sm < 1) blocks_per_sm = 1;
-  const uint64_t need = (p.nfull + T - 1) / T;
-  const uint64_t cap = (uint64_t)c.sms * (uint64_t)blocks_per_sm;
-  const int grid = (int)(need < 1 ? 1 : (need < cap ? need : cap));
-  kernel<<<grid, T, smem, c.stream>>>(p);
-  info->kernel = ALGO == kRing ? "staged_ring" : "staged_tree";
-  info->grid = grid;
-  info->block = T;
-  info->smem = smem;
+  if (ALGO == kTree && c.prog_len > kMaxProg) return cudaErrorInvalidValue;
+  const uint64_t columns = p.nfull + (p.tail ? 1 : 0);
+  const uint64_t grid = (columns + kThreads - 1) / kThreads;
+  if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(p);
+  info->kernel = ALGO == kRing ? "pipelined_ring" : "pipelined_tree";
+  info->grid = (int)grid;
+  info->block = kThreads;
+  info->smem = sizeof(uint4) * kSlots * kThreads;
   return cudaGetLastError();
-}
-
-template <int DT, int OP, int ALGO>
-cudaError_t launch_generic_t(const Call& c, LaunchInfo* info) {
-  // 64 threads keep P * 64 * 16 bytes <= 128 KiB up to P = 128; beyond that 32.
-  if (c.P <= 128) return launch_generic_one<DT, OP, ALGO, 64>(c, info);
-  return launch_generic_one<DT, OP, ALGO, 32>(c, info);
 }
 
 template <int DT, int OP>
 cudaError_t launch_generic_algo(const Call& c, LaunchInfo* info) {
-  if (c.algo == kRing) return launch_generic_t<DT, OP, kRing>(c, info);
-  if (c.algo == kTree) return launch_generic_t<DT, OP, kTree>(c, info);
+  if (c.algo == kRing) return launch_generic_one<DT, OP, kRing>(c, info);
+  if (c.algo == kTree) return launch_generic_one<DT, OP, kTree>(c, info);
   return cudaErrorInvalidValue;
 }
 

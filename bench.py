@@ -55,6 +55,8 @@ WORKLOADS = {
                                 dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
     "p72_16MiB_int32_sum_ring": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
                                      dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
+    "p72_16MiB_int32_max_tree": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
+                                     dtype="i32", op="max", algo="tree", scale=1.0, seed=0),
     # smaller cases of the same kernels, sized for profiler captures (inputs still exceed L2)
     "p8_64MiB_bf16_tree": dict(P=8, count=32 * 1024 * 1024, kind="normal_bf16", sigma=1e-2,
                                dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
