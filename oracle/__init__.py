@@ -86,6 +86,12 @@ class Oracle:
         L.oracle_ring_chunk_len.restype = sz
         L.oracle_tree_split.argtypes = [sz, ctypes.c_int]
         L.oracle_tree_split.restype = sz
+        L.oracle_reduce_scatter.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), sz,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_float]
+        L.oracle_reduce_scatter.restype = ctypes.c_int
+        L.oracle_all_gather.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), sz,
+                                        ctypes.c_int]
+        L.oracle_all_gather.restype = ctypes.c_int
         self.lib = L
         self.path = path
 
@@ -125,6 +131,39 @@ class Oracle:
                                                  dtype, op, algo, scale, out.ctypes.data))
         return out
 
+    def reduce_scatter(self, sends, dtype: int, op: int = SUM, scale: float = 1.0):
+        """sends: P arrays of P * recvcount elements; returns P shards."""
+        P = len(sends)
+        total = int(sends[0].shape[0])
+        if total % P:
+            raise OracleError("reduce-scatter input length must be P * recvcount")
+        rc = total // P
+        want = NP_DTYPE[dtype]
+        sends = [np.ascontiguousarray(s) for s in sends]
+        for s in sends:
+            if s.dtype != want or s.shape != (total,):
+                raise OracleError("all send arrays must share dtype and length")
+        recvs = [np.zeros(rc, dtype=want) for _ in range(P)]
+        sp = (ctypes.c_void_p * P)(*[s.ctypes.data for s in sends])
+        rp = (ctypes.c_void_p * P)(*[r.ctypes.data for r in recvs])
+        _check(self.lib.oracle_reduce_scatter(P, sp, rp, rc, dtype, op, scale))
+        return recvs
+
+    def all_gather(self, sends, dtype: int):
+        """sends: P arrays of sendcount elements; returns P arrays of P * sendcount."""
+        P = len(sends)
+        sc = int(sends[0].shape[0])
+        want = NP_DTYPE[dtype]
+        sends = [np.ascontiguousarray(s) for s in sends]
+        for s in sends:
+            if s.dtype != want or s.shape != (sc,):
+                raise OracleError("all send arrays must share dtype and length")
+        recvs = [np.zeros(P * sc, dtype=want) for _ in range(P)]
+        sp = (ctypes.c_void_p * P)(*[s.ctypes.data for s in sends])
+        rp = (ctypes.c_void_p * P)(*[r.ctypes.data for r in recvs])
+        _check(self.lib.oracle_all_gather(P, sp, rp, sc, dtype))
+        return recvs
+
     def tree_expr(self, P: int, tree: int) -> str:
         buf = ctypes.create_string_buffer(64 * 1024)
         _check(self.lib.oracle_tree_expr(P, tree, buf, len(buf)))
@@ -163,6 +202,14 @@ def allreduce_sampled(*a, **k):
 
 def tree_expr(P: int, tree: int) -> str:
     return default().tree_expr(P, tree)
+
+
+def reduce_scatter(*a, **k):
+    return default().reduce_scatter(*a, **k)
+
+
+def all_gather(*a, **k):
+    return default().all_gather(*a, **k)
 
 
 def f32_to_bf16(x: float) -> int:

@@ -47,6 +47,18 @@
  *   Min / max: acc = (x < acc) ? x : acc (min), acc = (x > acc) ? x : acc
  *   (max), in fold order; on ties the earlier operand is kept.
  *
+ *   REDUCE-SCATTER ("NCCL, NIXL, and Distributed GPU Communication", section
+ *   "Reduce-scatter"): every rank holds P shards of recvcount elements; the
+ *   shards are reduced across ranks and rank s receives reduced shard s.
+ *   Shard s is folded in the ring order of all-reduce chunk s -- x_s, then
+ *   x_{s+1}, ..., x_{s+P-1} -- so that all-reduce = reduce-scatter +
+ *   all-gather holds bit for bit whenever the shard length is a whole number
+ *   of 16-byte vectors (then the all-reduce's chunks are exactly the shards).
+ *
+ *   ALL-GATHER (same page, section "All-gather"): rank s contributes
+ *   sendcount elements; every rank receives all P contributions back to back,
+ *   rank s's at offset s * sendcount.  A copy: no arithmetic.
+ *
  *   Epilogue: y = narrow(acc * scale) for floating types when scale != 1,
  *   y = narrow(acc) otherwise; narrow is RNE to bf16, identity for fp32.
  *   scale != 1 is rejected for int32 and for min / max.
@@ -288,5 +300,44 @@ int oracle_allreduce_sampled(int P, const void* vals, const size_t* idx, size_t 
         acc_t y = reduce_element(x, P, count, idx[i], dtype, op, algo, scale);
         store_narrowed(out, i, y, dtype);
     }
+    return 0;
+}
+
+/*
+ * Reduce-scatter of P ranks' buffers of P * recvcount elements: recv[s] (host
+ * pointer, recvcount elements) receives reduced shard s.  Returns 0, -1 for
+ * invalid arguments, -2 for a scale the op does not take.
+ */
+int oracle_reduce_scatter(int P, const void* const* send, void* const* recv, size_t recvcount,
+                          int dtype, int op, float scale) {
+    int rc = check_args(P, dtype, op, OR_ALGO_RING, scale);
+    if (rc) return rc;
+    acc_t x[OR_MAX_RANKS];
+    for (int s = 0; s < P; ++s) {
+        for (size_t i = 0; i < recvcount; ++i) {
+            size_t e = (size_t)s * recvcount + i;
+            for (int r = 0; r < P; ++r) x[r] = load_widened(send[r], e, dtype);
+            acc_t acc = x[s];
+            for (int k = 1; k < P; ++k) acc = combine(acc, x[(s + k) % P], dtype, op);
+            if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;
+            store_narrowed(recv[s], i, acc, dtype);
+        }
+    }
+    return 0;
+}
+
+/*
+ * All-gather: recv[r] (P * sendcount elements) receives send[0], ..., send[P-1]
+ * back to back, for every rank r.
+ */
+int oracle_all_gather(int P, const void* const* send, void* const* recv, size_t sendcount,
+                      int dtype) {
+    if (P < 1 || P > OR_MAX_RANKS || elem_size(dtype) == 0) return -1;
+    size_t es = elem_size(dtype);
+    for (int r = 0; r < P; ++r)
+        for (int s = 0; s < P; ++s)
+            for (size_t i = 0; i < sendcount; ++i)
+                memcpy((char*)recv[r] + ((size_t)s * sendcount + i) * es,
+                       (const char*)send[s] + i * es, es);
     return 0;
 }

@@ -460,6 +460,137 @@ def pin_sampled_matches_full(O):
                                full[idx], f"sampled P={P} dtype={dtype} algo={algo} op={op}")
 
 
+# ------------------------------------------- reduce-scatter and all-gather
+
+def _golden(name):
+    spec = {"before": {}, "after": {}}
+    nranks = None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *rest = line.split()
+            if key == "ranks":
+                nranks = int(rest[0])
+            else:
+                spec[key][int(rest[0])] = rest[1:]
+    return nranks, spec
+
+
+def ring_reduce_scatter_steps(sends, dtype: int, op: int, scale: float):
+    """Reduce-scatter run literally on a ring: shard s starts at rank s and
+    travels s -> s+1 -> ...; at step k (0 .. P-2) rank r passes its partial of
+    shard (r - k) mod P to rank r+1, which combines (partial) (+) (own).  After
+    P-1 steps shard s is complete at rank s-1, which scales and narrows it
+    and hands it to rank s."""
+    P = len(sends)
+    rc = len(sends[0]) // P
+    buf = [widened(s, dtype) for s in sends]
+    for k in range(P - 1):
+        msgs = []
+        for r in range(P):
+            sh = (r - k) % P
+            msgs.append(((r + 1) % P, sh, buf[r][sh * rc:(sh + 1) * rc]))
+        for dst, sh, data in msgs:
+            for i in range(rc):
+                e = sh * rc + i
+                buf[dst][e] = combine(data[i], buf[dst][e], dtype, op)
+    return [narrow(buf[(sh - 1) % P][sh * rc:(sh + 1) * rc], dtype, scale) for sh in range(P)]
+
+
+def pin_reduce_scatter_worked_example(O):
+    """Golden: "NCCL, NIXL, ...", section "Reduce-scatter"."""
+    n, spec = _golden("worked_example_reduce_scatter_p4.txt")
+    assert n == 4
+    rng = np.random.default_rng(41)
+    rc = 257
+    for dtype, lim in ((F32, 1 << 20), (I32, 1 << 20), (BF16, 32)):
+        ints = {spec["before"][r][0]: rng.integers(-lim, lim + 1, size=4 * rc) for r in range(4)}
+        sends = [(bf16_bits_torch(v.astype(np.float32)) if dtype == BF16 else v.astype(NP_DTYPE[dtype]))
+                 for v in (ints[spec["before"][r][0]] for r in range(4))]
+        out = O.reduce_scatter(sends, dtype, SUM)
+        for r in range(4):
+            words = spec["after"][r]
+            assert words[0] == "shard" and words[2] == "of"
+            sh = int(words[1])
+            exact = sum(ints[t] for t in words[3].split("+"))[sh * rc:(sh + 1) * rc]
+            want = exact.astype(np.int32) if dtype == I32 else exact.astype(np.float32)
+            if dtype == BF16:
+                want = bf16_bits_torch(want)
+            assert_bitwise(out[r], want, f"reduce-scatter example dtype={dtype} rank={r}")
+
+
+def pin_all_gather_worked_example(O):
+    """Golden: "NCCL, NIXL, ...", section "All-gather"."""
+    n, spec = _golden("worked_example_all_gather_p4.txt")
+    assert n == 4
+    rng = np.random.default_rng(43)
+    for dtype in (F32, BF16, I32):
+        x = {spec["before"][r][0]: random_inputs(rng, 1, 33, dtype)[0] for r in range(4)}
+        out = O.all_gather([x[spec["before"][r][0]] for r in range(4)], dtype)
+        for r in range(4):
+            want = np.concatenate([x[sym] for sym in spec["after"][r]])
+            assert_bitwise(out[r], want, f"all-gather example dtype={dtype} rank={r}")
+
+
+def pin_allreduce_is_reduce_scatter_then_all_gather(O):
+    """All-reduce = reduce-scatter + all-gather ("NCCL, NIXL, ...", section
+    "Reduce-scatter"), bit for bit when each shard is whole 16-byte vectors."""
+    rng = np.random.default_rng(47)
+    for P in (1, 2, 3, 4, 8, 9):
+        for dtype in (F32, BF16, I32):
+            rc = VEC[dtype] * 5
+            sends = random_inputs(rng, P, P * rc, dtype)
+            for op in (SUM, MIN, MAX):
+                scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                for scale in scales:
+                    shards = O.reduce_scatter(sends, dtype, op, scale)
+                    gathered = O.all_gather(shards, dtype)
+                    ar = O.allreduce(sends, dtype, op, RING, scale)
+                    for r in range(P):
+                        assert_bitwise(gathered[r], ar[r], f"RS+AG vs AR P={P} dtype={dtype} "
+                                                           f"op={op} scale={scale} rank={r}")
+
+
+def pin_reduce_scatter_ring_steps(O):
+    rng = np.random.default_rng(53)
+    for P in (1, 2, 3, 5, 8):
+        for rc in (1, 3, 6):
+            for dtype in (F32, BF16, I32):
+                sends = random_inputs(rng, P, P * rc, dtype)
+                for op in (SUM, MIN, MAX):
+                    scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                    for scale in scales:
+                        want = ring_reduce_scatter_steps(sends, dtype, op, scale)
+                        got = O.reduce_scatter(sends, dtype, op, scale)
+                        for r in range(P):
+                            assert_bitwise(got[r], want[r], f"RS ring steps P={P} rc={rc} "
+                                                            f"dtype={dtype} op={op} rank={r}")
+
+
+def pin_collectives_order_independent(O):
+    rng = np.random.default_rng(59)
+    for P in (2, 7, 72):
+        rc = 11
+        sends = random_inputs(rng, P, P * rc, I32)
+        wide = np.stack([x.astype(np.int64) for x in sends])
+        total = wide.sum(axis=0) & 0xFFFFFFFF
+        total = np.where(total >= 2 ** 31, total - 2 ** 32, total).astype(np.int32)
+        shards = O.reduce_scatter(sends, I32, SUM)
+        for r in range(P):
+            assert_bitwise(shards[r], total[r * rc:(r + 1) * rc], f"RS int sum P={P} rank={r}")
+        mx = O.reduce_scatter(sends, I32, MAX)
+        for r in range(P):
+            assert_bitwise(mx[r], wide.max(axis=0)[r * rc:(r + 1) * rc].astype(np.int32),
+                           f"RS int max P={P} rank={r}")
+        gathered = O.all_gather([x[:rc] for x in sends], I32)
+        for r in range(P):
+            assert_bitwise(gathered[r], np.concatenate([x[:rc] for x in sends]), f"AG P={P} rank={r}")
+
+
 ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_tree_expressions,
             pin_tree_structure, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
-            pin_sampled_matches_full]
+            pin_sampled_matches_full, pin_reduce_scatter_worked_example, pin_all_gather_worked_example,
+            pin_allreduce_is_reduce_scatter_then_all_gather, pin_reduce_scatter_ring_steps,
+            pin_collectives_order_independent]

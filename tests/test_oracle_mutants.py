@@ -15,7 +15,8 @@ import pins
 MUTANTS = {
     "ring_direction": ("x[(c + k) % P]", "x[(c + P - k) % P]"),
     "ring_start_rank": ("int c = (int)(e / L);", "int c = (int)((e / L + 1) % (size_t)P);"),
-    "ring_dropped_rank": ("for (int k = 1; k < P; ++k)", "for (int k = 1; k < P - 1; ++k)"),
+    "ring_dropped_rank": ("for (int k = 1; k < P; ++k) acc = combine(acc, x[(c + k) % P]",
+                          "for (int k = 1; k < P - 1; ++k) acc = combine(acc, x[(c + k) % P]"),
     "chunk_not_16B": ("return round_up(per, vec_elems(dtype));", "return per;"),
     "sum_sign": ("acc.f = acc.f + x.f;", "acc.f = acc.f - x.f;"),
     "min_flipped": ("acc.f = (x.f < acc.f) ? x.f : acc.f;", "acc.f = (x.f > acc.f) ? x.f : acc.f;"),
@@ -39,10 +40,18 @@ MUTANTS = {
                          "size_t h = round_up(count / 2, vec_elems(dtype));"),
     "rne_ties_away": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;",
                       "if (lower >= 0x8000u) upper += 1;"),
-    "scale_dropped": ("if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;", ""),
+    "scale_dropped": ("    if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;\n    return acc;",
+                      "    return acc;"),
     "only_rank0_written": ("for (int r = 0; r < P; ++r) store_narrowed(recv[r], e, y, dtype);",
                            "store_narrowed(recv[0], e, y, dtype);"),
     "bf16_widen_shift": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
+    "rs_shard_start": ("            acc_t acc = x[s];\n            for (int k = 1; k < P; ++k) acc = combine(acc, x[(s + k) % P], dtype, op);",
+                       "            acc_t acc = x[(s + 1) % P];\n            for (int k = 2; k <= P; ++k) acc = combine(acc, x[(s + k) % P], dtype, op);"),
+    "rs_wrong_shard": ("            size_t e = (size_t)s * recvcount + i;", "            size_t e = (size_t)((s + 1) % P) * recvcount + i;"),
+    "rs_scale_dropped": ("            if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;\n            store_narrowed(recv[s], i, acc, dtype);",
+                         "            store_narrowed(recv[s], i, acc, dtype);"),
+    "ag_wrong_offset": ("memcpy((char*)recv[r] + ((size_t)s * sendcount + i) * es,",
+                        "memcpy((char*)recv[r] + ((size_t)((s + r) % P) * sendcount + i) * es,"),
 }
 
 
