@@ -72,6 +72,11 @@ def library() -> ctypes.CDLL:
                 L.ar_select_algo.restype = i
                 L.ar_set_option.argtypes = [vp, i, ctypes.c_longlong]
                 L.ar_set_option.restype = i
+                L.ar_reduce_scatter.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i, i,
+                                                 ctypes.c_float, vp]
+                L.ar_reduce_scatter.restype = i
+                L.ar_all_gather.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i, vp]
+                L.ar_all_gather.restype = i
                 L.ar_allreduce_ll_noalloc.argtypes = [i, ctypes.POINTER(vp), ctypes.POINTER(vp), sz,
                                                       i, i, ctypes.c_float, vp, ctypes.POINTER(i)]
                 L.ar_allreduce_ll_noalloc.restype = i
@@ -124,6 +129,32 @@ def ar_allreduce(comm: int, sendbufs, recvbufs, count: int, dtype: int, op: int 
                                 float(scale), _stream_handle(stream))
     if st != AR_SUCCESS:
         raise ArError(st, "ar_allreduce")
+
+
+def ar_reduce_scatter(comm: int, sendbufs, recvbufs, recvcount: int, dtype: int, op: int = AR_SUM,
+                      scale: float = 1.0, stream=None) -> None:
+    """sendbufs: P buffers of P * recvcount elements; recvbufs[s] gets shard s."""
+    P = len(sendbufs)
+    if len(recvbufs) != P:
+        raise ArError(AR_ERR_INVALID_ARG, "ar_reduce_scatter: sendbufs and recvbufs differ in length")
+    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
+    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    st = library().ar_reduce_scatter(comm, sp, rp, int(recvcount), int(dtype), int(op), float(scale),
+                                     _stream_handle(stream))
+    if st != AR_SUCCESS:
+        raise ArError(st, "ar_reduce_scatter")
+
+
+def ar_all_gather(comm: int, sendbufs, recvbufs, sendcount: int, dtype: int, stream=None) -> None:
+    """sendbufs: P buffers of sendcount elements; every recvbufs[r] gets all P of them."""
+    P = len(sendbufs)
+    if len(recvbufs) != P:
+        raise ArError(AR_ERR_INVALID_ARG, "ar_all_gather: sendbufs and recvbufs differ in length")
+    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
+    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    st = library().ar_all_gather(comm, sp, rp, int(sendcount), int(dtype), _stream_handle(stream))
+    if st != AR_SUCCESS:
+        raise ArError(st, "ar_all_gather")
 
 
 def ar_get_status(comm: int) -> int:

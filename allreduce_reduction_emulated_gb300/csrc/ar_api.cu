@@ -111,6 +111,84 @@ bool overlapping(const void* const* send, void* const* recv, int P, size_t bytes
   return false;
 }
 
+// Reduce-scatter / all-gather layouts: the P big buffers hold P * shard
+// elements, the P small ones shard elements.  Two buffers may share memory
+// only when they are identical or in the in-place layout, where rank r's
+// small buffer sits at element offset r * shard inside rank r's big buffer.
+bool bad_shard_layout(const void* const* big, const void* const* small, int P, size_t shard_bytes) {
+  struct Span {
+    uintptr_t lo, hi;
+    int rank;
+    bool is_big;
+  };
+  std::vector<Span> v;
+  v.reserve(2 * (size_t)P);
+  for (int r = 0; r < P; ++r) {
+    v.push_back({(uintptr_t)big[r], (uintptr_t)big[r] + (uintptr_t)P * shard_bytes, r, true});
+    v.push_back({(uintptr_t)small[r], (uintptr_t)small[r] + shard_bytes, r, false});
+  }
+  std::sort(v.begin(), v.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+  for (size_t i = 0; i < v.size(); ++i) {
+    for (size_t j = i + 1; j < v.size() && v[j].lo < v[i].hi; ++j) {
+      const Span& a = v[i];
+      const Span& b = v[j];
+      if (a.lo == b.lo && a.hi == b.hi) continue;  // identical buffers
+      const Span& bg = a.is_big ? a : b;
+      const Span& sm = a.is_big ? b : a;
+      if (bg.is_big && !sm.is_big && bg.rank == sm.rank &&
+          sm.lo == bg.lo + (uintptr_t)sm.rank * shard_bytes)
+        continue;  // in place
+      return true;
+    }
+  }
+  return false;
+}
+
+// Pointers need element alignment; *vec is set when every pointer and the
+// shard size are whole 16-byte units (the vector kernels' condition).
+ar_status_t check_collective(ar_comm_t c, const void* const* a, const void* const* b, ar_dtype_t dtype,
+                             size_t shard, bool* vec) {
+  if (!valid_dtype(dtype)) return AR_ERR_INVALID_ARG;
+  if (shard == 0) return AR_SUCCESS;
+  if (!a || !b) return AR_ERR_INVALID_ARG;
+  const size_t es = ar::elem_bytes(dtype);
+  if (shard > ((size_t)1 << 62) / es / (size_t)c->P) return AR_ERR_INVALID_ARG;
+  uintptr_t bits = (uintptr_t)(shard * es);
+  for (int r = 0; r < c->P; ++r) {
+    if (!a[r] || !b[r]) return AR_ERR_INVALID_ARG;
+    if (((uintptr_t)a[r] | (uintptr_t)b[r]) & (es - 1)) return AR_ERR_INVALID_ARG;
+    bits |= (uintptr_t)a[r] | (uintptr_t)b[r];
+  }
+  *vec = (bits & 15u) == 0;
+  if (bad_shard_layout(a, b, c->P, shard * es)) return AR_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  return dev == c->device ? AR_SUCCESS : AR_ERR_INVALID_ARG;
+}
+
+ar::Call base_call(ar_comm_t c, void* stream) {
+  ar::Call call;
+  call.P = c->P;
+  call.stream = static_cast<cudaStream_t>(stream);
+  call.sms = c->sms;
+  call.tree_prog = c->tree_prog;
+  call.prog_len = c->prog_len;
+  call.staging = c->staging;
+  call.stage_stride = c->stage_stride;
+  call.status = c->status;
+  call.spin_limit = c->spin_limit;
+  call.skip_produce = c->skip_produce;
+  call.epoch = 0;
+  call.shard = 0;
+  call.algo = ar::kRing;
+  call.scale = 1.0f;
+  call.op = AR_SUM;
+  return call;
+}
+
 }  // namespace
 
 extern "C" {
@@ -281,6 +359,7 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   call.spin_limit = c->spin_limit;
   call.skip_produce = c->skip_produce;
   call.epoch = 0;
+  call.shard = 0;
 
   ar::LaunchInfo info;
   cudaError_t e;
@@ -312,6 +391,61 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
                  info.kernel, info.grid, info.block, info.smem, count * esize, call.epoch,
                  cudaGetErrorString(e));
   }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  return AR_SUCCESS;
+}
+
+ar_status_t ar_reduce_scatter(ar_comm_t c, const void* const* sendbufs, void* const* recvbufs,
+                              size_t recvcount, ar_dtype_t dtype, ar_op_t op, float scale,
+                              void* stream) {
+  if (!c || !valid_op(op)) return AR_ERR_INVALID_ARG;
+  if (!(scale == scale)) return AR_ERR_INVALID_ARG;
+  if (scale != 1.0f && (dtype == AR_INT32 || op != AR_SUM)) return AR_ERR_UNSUPPORTED;
+  bool vec = false;
+  ar_status_t st = check_collective(c, sendbufs, (const void* const*)recvbufs, dtype, recvcount, &vec);
+  if (st != AR_SUCCESS || recvcount == 0) return st;
+  ar::Call call = base_call(c, stream);
+  call.send = sendbufs;
+  call.recv = recvbufs;
+  call.count = (size_t)c->P * recvcount;
+  call.shard = recvcount;
+  call.dtype = dtype;
+  call.op = op;
+  call.scale = scale;
+  ar::LaunchInfo info;
+  cudaError_t e = vec ? ar::launch_reduce_scatter_vec(call, &info) : ar::launch_reduce_scatter_elem(call, &info);
+  if (c->debug)
+    std::fprintf(stderr, "[ar] reduce_scatter P=%d recvcount=%zu dtype=%s op=%s kernel=%s grid=%d status=%s\n",
+                 c->P, recvcount, dtype_name(dtype), op_name(op), info.kernel, info.grid,
+                 cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  return AR_SUCCESS;
+}
+
+ar_status_t ar_all_gather(ar_comm_t c, const void* const* sendbufs, void* const* recvbufs,
+                          size_t sendcount, ar_dtype_t dtype, void* stream) {
+  if (!c) return AR_ERR_INVALID_ARG;
+  bool vec = false;
+  ar_status_t st = check_collective(c, (const void* const*)recvbufs, sendbufs, dtype, sendcount, &vec);
+  if (st != AR_SUCCESS || sendcount == 0) return st;
+  ar::Call call = base_call(c, stream);
+  call.send = sendbufs;
+  call.recv = recvbufs;
+  call.count = (size_t)c->P * sendcount;
+  call.shard = sendcount;
+  call.dtype = dtype;
+  call.algo = vec ? 1 : 0;  // 1: 16-byte vector copy
+  ar::LaunchInfo info;
+  cudaError_t e = ar::launch_all_gather(call, &info);
+  if (c->debug)
+    std::fprintf(stderr, "[ar] all_gather P=%d sendcount=%zu dtype=%s kernel=%s grid=%d status=%s\n",
+                 c->P, sendcount, dtype_name(dtype), info.kernel, info.grid, cudaGetErrorString(e));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return AR_ERR_CUDA;

@@ -65,21 +65,29 @@ __device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ops, int 
     for (int k = 1; k < P; ++k) fold<DT, OP>(acc, next());
     return acc;
   } else {
+    // the stack's top entry lives in registers; only deeper entries go to
+    // the (local-memory) array: a push stores the old top, a combine loads
+    // the entry below and folds the top into it
     Acc<DT> stack[kStackDepth];
-    int sp = 0;
-    for (int i = 0; i < nops; ++i) {
+    Acc<DT> top = next();  // a program always starts with a push
+    int sp = 0;            // entries below the top
+    for (int i = 1; i < nops; ++i) {
       if (ops[i] >= 0) {
-        stack[sp++] = next();
+        stack[sp++] = top;
+        top = next();
       } else {
-        --sp;
-        fold<DT, OP>(stack[sp - 1], stack[sp]);
+        Acc<DT> below = stack[--sp];
+        fold<DT, OP>(below, top);
+        top = below;
       }
     }
-    return stack[0];
+    return top;
   }
 }
 
-template <int DT, int OP, int ALGO>
+// SCATTER (ring only): reduce-scatter -- chunk c is shard c and its result
+// goes only to rank c's receive buffer, at the shard-relative position.
+template <int DT, int OP, int ALGO, bool SCATTER = false>
 __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __grid_constant__ GenericParams p) {
   __shared__ uint4 slots[kSlots][kThreads];
   __shared__ const uint4* s_send[AR_MAX_RANKS];
@@ -147,7 +155,11 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     acc = fold_sequence<DT, OP, ALGO>(P, ops, p.prog_len, next);
     cp_async_wait<0>();
     const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
-    for (int r = 0; r < P; ++r) st_stream(s_recv[r] + v, o);
+    if constexpr (SCATTER) {
+      st_stream(s_recv[first] + (v - (uint64_t)first * p.split), o);
+    } else {
+      for (int r = 0; r < P; ++r) st_stream(s_recv[r] + v, o);
+    }
   } else {
     // the trailing partial vector: element-wise loads, same order
     int j = 0;
@@ -204,7 +216,54 @@ cudaError_t launch_generic_op(const Call& c, LaunchInfo* info) {
   }
 }
 
+template <int DT, int OP>
+cudaError_t launch_scatter_one(const Call& c, LaunchInfo* info) {
+  auto kernel = generic_allreduce_kernel<DT, OP, kRing, true>;
+  GenericParams p;
+  for (int r = 0; r < c.P; ++r) {
+    p.send[r] = static_cast<const uint4*>(c.send[r]);
+    p.recv[r] = static_cast<uint4*>(c.recv[r]);
+  }
+  p.prog = nullptr;
+  p.prog_len = 0;
+  p.P = c.P;
+  const uint64_t V = (uint64_t)vec_elems(DT);
+  if (c.shard % V != 0) return cudaErrorInvalidValue;  // whole vectors per shard only
+  p.nfull = c.count / V;
+  p.tail = 0;
+  p.split = c.shard / V;
+  p.scale = c.scale;
+  p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
+  const uint64_t grid = (p.nfull + kThreads - 1) / kThreads;
+  if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
+  kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(p);
+  info->kernel = "pipelined_reduce_scatter";
+  info->grid = (int)grid;
+  info->block = kThreads;
+  info->smem = sizeof(uint4) * kSlots * kThreads;
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_scatter_op(const Call& c, LaunchInfo* info) {
+  switch (c.op) {
+    case kSum: return launch_scatter_one<DT, kSum>(c, info);
+    case kMin: return launch_scatter_one<DT, kMin>(c, info);
+    case kMax: return launch_scatter_one<DT, kMax>(c, info);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_reduce_scatter_vec(const Call& c, LaunchInfo* info) {
+  switch (c.dtype) {
+    case kF32: return launch_scatter_op<kF32>(c, info);
+    case kBF16: return launch_scatter_op<kBF16>(c, info);
+    case kI32: return launch_scatter_op<kI32>(c, info);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_generic(const Call& c, LaunchInfo* info) {
   switch (c.dtype) {

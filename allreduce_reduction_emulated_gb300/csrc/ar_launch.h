@@ -30,6 +30,9 @@ struct Call {
   unsigned long long* staging;  // P slots of stage_stride 8-byte words
   size_t stage_stride;
   int* status;                  // device status word (ar_status_t)
+  // reduce-scatter / all-gather: elements per shard (recvcount / sendcount);
+  // count is then the length of the larger buffers (P * shard)
+  size_t shard;
   uint32_t epoch;
   uint32_t spin_limit;
   int skip_produce;
@@ -52,6 +55,12 @@ cudaError_t launch_static_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
 cudaError_t launch_generic(const Call& c, LaunchInfo* info);
 cudaError_t launch_ll(const Call& c, LaunchInfo* info);
+// reduce-scatter with shards of whole 16-byte vectors (pipelined ring kernel)
+cudaError_t launch_reduce_scatter_vec(const Call& c, LaunchInfo* info);
+// reduce-scatter of any shard length, element by element (same order)
+cudaError_t launch_reduce_scatter_elem(const Call& c, LaunchInfo* info);
+// all-gather: every rank's shard copied to all P receive buffers
+cudaError_t launch_all_gather(const Call& c, LaunchInfo* info);
 
 // Ring chunk length in vectors and first vector of tree 1, for `count`.
 inline uint64_t ring_chunk_vectors(size_t count, int P, int dtype) {

@@ -64,7 +64,24 @@ WORKLOADS = {
                                     dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
     "p8_4KiB_fp32_ll": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
                             algo="ll", scale=1.0, seed=0),
+    # the ring's two halves as standalone collectives: count = elements per shard
+    "p8_rs_8MiB_shards_fp32": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
+                                   op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter"),
+    "p8_ag_8MiB_shards_fp32": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
+                                   op="sum", algo="ring", scale=1.0, seed=0, coll="all_gather"),
 }
+
+
+def sizes_of(w: dict):
+    """(elements per input buffer, per output buffer, nccl-tests size in bytes,
+    busbw factor, HBM bytes per call) of a workload."""
+    P, n, es = w["P"], w["count"], ESIZE[w["dtype"]]
+    coll = w.get("coll", "allreduce")
+    if coll == "reduce_scatter":
+        return P * n, n, P * n * es, (P - 1) / P, P * P * n * es + P * n * es
+    if coll == "all_gather":
+        return n, P * n, P * n * es, (P - 1) / P, P * n * es + P * P * n * es
+    return n, n, n * es, 2 * (P - 1) / P, 2 * P * n * es
 ESIZE = {"f32": 4, "bf16": 2, "i32": 4}
 
 # DDP-style bucketed run: 24 layers of [2048x8192], [8192x2048], [2048x6144],
@@ -91,7 +108,8 @@ def parse_args():
 
 
 def config_of(name: str, w: dict, n: int) -> dict:
-    return {"workload": name, "P": w["P"], "count_per_rank": w["count"], "dtype": w["dtype"],
+    return {"workload": name, "collective": w.get("coll", "allreduce"), "P": w["P"],
+            "count_per_rank": w["count"], "dtype": w["dtype"],
             "op": w["op"], "algo": w["algo"], "scale": w["scale"],
             "values": f"{w['kind']} sigma={w['sigma']} seed={w['seed']}",
             "l2": "inputs larger than L2 (no flush)" if 2 * w["P"] * w["count"] * ESIZE[w["dtype"]] > 2 * 129e6
@@ -230,19 +248,27 @@ def oracle_throughput(w: dict, host_sends, seconds: float):
     import oracle
 
     P, count = w["P"], w["count"]
+    coll = w.get("coll", "allreduce")
     dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
     op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
     algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL}[w["algo"]]
-    recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
-    oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, min(count, 65536), recvs)  # warm
+    nccl_bytes = sizes_of(w)[2]
+    if coll == "allreduce":
+        recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
+        oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, min(count, 65536), recvs)  # warm
     done, t0 = 0, time.perf_counter()
     while True:
-        oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, count, recvs)
-        done += count
+        if coll == "reduce_scatter":
+            oracle.reduce_scatter(host_sends, dt, op, w["scale"])
+        elif coll == "all_gather":
+            oracle.all_gather(host_sends, dt)
+        else:
+            oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, count, recvs)
+        done += 1
         el = time.perf_counter() - t0
-        if el >= seconds or done >= 8 * count:
+        if el >= seconds or done >= 8:
             break
-    return done * ESIZE[w["dtype"]] / el / 1e9, done // count, el
+    return done * nccl_bytes / el / 1e9, done, el
 
 
 def reference_arm(args, w, name):
@@ -255,6 +281,8 @@ def reference_arm(args, w, name):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    if w.get("coll", "allreduce") != "allreduce":
+        raise SystemExit("--impl reference times the all-reduce workloads")
     P, count = w["P"], w["count"]
     dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
     op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
@@ -330,13 +358,23 @@ def ours_arm(args, w, name):
     dtype = {"f32": ar.AR_FLOAT32, "bf16": ar.AR_BFLOAT16, "i32": ar.AR_INT32}[w["dtype"]]
     op = ar.OPS[w["op"]]
     algo = ar.ALGOS[w["algo"]]
-    sends = [synthetic.values_torch(w["kind"], w["seed"], r, 0, count, dev, w["sigma"]) for r in range(P)]
-    recvs = [torch.empty_like(s) for s in sends]
+    coll = w.get("coll", "allreduce")
+    n_in, n_out, nccl_bytes, bus_factor, hbm_bytes = sizes_of(w)
+    sends = [synthetic.values_torch(w["kind"], w["seed"], r, 0, n_in, dev, w["sigma"]) for r in range(P)]
+    recvs = [torch.empty(n_out, dtype=sends[0].dtype, device=dev) for _ in range(P)]
     comm = ar.ar_init(P)
     stream = torch.cuda.current_stream()
 
+    def call(xs, ys, s):
+        if coll == "reduce_scatter":
+            ar.ar_reduce_scatter(comm, xs, ys, count, dtype, op, w["scale"], s)
+        elif coll == "all_gather":
+            ar.ar_all_gather(comm, xs, ys, count, dtype, s)
+        else:
+            ar.ar_allreduce(comm, xs, ys, count, dtype, op, algo, w["scale"], s)
+
     def step():
-        ar.ar_allreduce(comm, sends, recvs, count, dtype, op, algo, w["scale"], stream)
+        call(sends, recvs, stream)
 
     for _ in range(args.warmup):
         step()
@@ -369,8 +407,7 @@ def ours_arm(args, w, name):
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error in the timed region")
     ms_step = max_over_ranks(ms, dist) / args.steps
-    algbw = job_gbs(count * esize, ms_step, world)
-    hbm_bytes = 2 * P * count * esize
+    algbw = job_gbs(nccl_bytes, ms_step, world)
     achieved = hbm_bytes / (ms_step * 1e-3) / 1e9           # one kernel per step
     peak, peak_kind = measured_hbm_peak()
 
@@ -379,8 +416,8 @@ def ours_arm(args, w, name):
     # results back.  Steps are pipelined over two device buffer sets and three
     # streams (H2D of step i+1 and D2H of step i-1 overlap the call of step i).
     host_in = [s.cpu().pin_memory() for s in sends]
-    host_out = [torch.empty_like(h).pin_memory() for h in host_in]
-    sets = [(sends, recvs), ([torch.empty_like(s) for s in sends], [torch.empty_like(s) for s in sends])]
+    host_out = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in recvs]
+    sets = [(sends, recvs), ([torch.empty_like(s) for s in sends], [torch.empty_like(s) for s in recvs])]
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     nsteps = args.e2e_steps
 
@@ -404,7 +441,7 @@ def ours_arm(args, w, name):
             s_run.wait_event(ready)
             if i >= 2:
                 s_run.wait_event(done_out[i - 2])    # step i-2's results have left
-            ar.ar_allreduce(comm, d_in, d_out, count, dtype, op, algo, w["scale"], s_run)
+            call(d_in, d_out, s_run)
             done_run[i] = torch.cuda.Event()
             done_run[i].record(s_run)
             s_out.wait_event(done_run[i])
@@ -423,7 +460,7 @@ def ours_arm(args, w, name):
     e2e_ms = max_over_ranks(e2e_run(nsteps) / nsteps, dist)
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error in the end-to-end run")
-    e2e_value = job_gbs(count * esize, e2e_ms, world)
+    e2e_value = job_gbs(nccl_bytes, e2e_ms, world)
 
     line = None
     if rank == 0:
@@ -433,7 +470,7 @@ def ours_arm(args, w, name):
                        for h in host_in]
             gbs, passes, el = oracle_throughput(w, host_np, args.cpu_seconds)
             cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{passes} full pass(es) over the workload ({P} x {count} elements), "
+                   "sample": f"{passes} full pass(es) over the workload ({P} x {n_in} input elements), "
                              f"{el:.1f} s on one host core"}
         traffic = profiled_traffic(name)
         line = {
@@ -441,14 +478,14 @@ def ours_arm(args, w, name):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
             "config": config_of(name, w, world),
-            "busbw": algbw * 2 * (P - 1) / P,
+            "busbw": algbw * bus_factor,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "algorithmic_bytes_per_launch": hbm_bytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "steps": nsteps, "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": P * count * esize, "d2h_bytes_per_step": P * count * esize,
+                    "h2d_bytes_per_step": P * n_in * esize, "d2h_bytes_per_step": P * n_out * esize,
                     "path": "pinned host -> device copies, ar_allreduce, device -> pinned host copies "
                             "of all P results; pipelined over 2 buffer sets / 3 streams"},
             "gpu_launches": args.steps,

@@ -154,6 +154,45 @@ typedef enum {
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
 
 /*
+ * Reduce-scatter ("NCCL, NIXL, and Distributed GPU Communication", section
+ * "Reduce-scatter": the ranks' values are reduced and the result is split
+ * into P shards, rank s receiving shard s).
+ *   sendbufs  P device pointers to P * recvcount elements each (rank r's
+ *             full vector)
+ *   recvbufs  P device pointers to recvcount elements: recvbufs[s] receives
+ *             reduced shard s
+ * Shard s is folded in the ring order of all-reduce chunk s (x_s, then
+ * x_{s+1}, ..., x_{s+P-1}); so when recvcount * sizeof(element) is a
+ * multiple of 16, reduce-scatter followed by all-gather equals ar_allreduce
+ * with AR_ALGO_RING bit for bit ("all-reduce = reduce-scatter + all-gather").
+ * op, scale, stream, asynchrony and errors as for ar_allreduce.  Pointers
+ * need only element alignment here; when every pointer and recvcount *
+ * sizeof(element) are multiples of 16 bytes the 16-byte vector kernel runs,
+ * otherwise an element-wise kernel with the same order.  Buffers may share
+ * memory only when identical or in place (recvbufs[r] == sendbufs[r] +
+ * r * recvcount elements).  recvcount == 0 is a no-op.
+ */
+ar_status_t ar_reduce_scatter(ar_comm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                              size_t recvcount, ar_dtype_t dtype, ar_op_t op, float scale,
+                              void* stream);
+
+/*
+ * All-gather (same page, section "All-gather": every rank receives all
+ * ranks' pieces, k ranks of N values giving k x N values on every rank).
+ *   sendbufs  P device pointers to sendcount elements (rank s's piece)
+ *   recvbufs  P device pointers to P * sendcount elements: every rank
+ *             receives piece s at element offset s * sendcount
+ * A copy (no arithmetic; dtype only sets the element size).  Pointers need
+ * only element alignment (16-byte vectors are used when every pointer and
+ * sendcount * sizeof(element) are multiples of 16).  Buffers may share memory
+ * only when identical or in place (sendbufs[r] == recvbufs[r] + r * sendcount
+ * elements).  Stream, asynchrony and errors as for ar_allreduce; sendcount
+ * == 0 is a no-op.
+ */
+ar_status_t ar_all_gather(ar_comm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                          size_t sendcount, ar_dtype_t dtype, void* stream);
+
+/*
  * LL all-reduce that allocates nothing.  (The pages have no counterpart: this
  * entry point exists for callers of this library that cannot allocate device
  * memory -- code whose device memory belongs to a framework's pool, code in a
