@@ -57,9 +57,10 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Folds the column in the algorithm's order; next() yields the widened
-// input of the next rank in the push sequence.
+// input of the next rank in the push sequence.  The tree runs as P pushes,
+// push j followed by ncomb[j] combines (the postorder program regrouped).
 template <int DT, int OP, int ALGO, class Next>
-__device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ops, int nops, Next& next) {
+__device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ncomb, Next& next) {
   if constexpr (ALGO == kRing) {
     Acc<DT> acc = next();
     for (int k = 1; k < P; ++k) fold<DT, OP>(acc, next());
@@ -69,13 +70,12 @@ __device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ops, int 
     // the (local-memory) array: a push stores the old top, a combine loads
     // the entry below and folds the top into it
     Acc<DT> stack[kStackDepth];
-    Acc<DT> top = next();  // a program always starts with a push
+    Acc<DT> top = next();  // push 0 (never followed by a combine)
     int sp = 0;            // entries below the top
-    for (int i = 1; i < nops; ++i) {
-      if (ops[i] >= 0) {
-        stack[sp++] = top;
-        top = next();
-      } else {
+    for (int j = 1; j < P; ++j) {
+      stack[sp++] = top;
+      top = next();
+      for (int c = ncomb[j]; c > 0; --c) {
         Acc<DT> below = stack[--sp];
         fold<DT, OP>(below, top);
         top = below;
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
   __shared__ const uint4* s_send[AR_MAX_RANKS];
   __shared__ uint4* s_recv[AR_MAX_RANKS];
   __shared__ int16_t s_prog[2][kMaxProg];   // tree programs
-  __shared__ int16_t s_push[2][AR_MAX_RANKS];  // tree leaf (push) sequences
+  __shared__ int16_t s_push[2][AR_MAX_RANKS];   // tree leaf (push) sequences
+  __shared__ int16_t s_ncomb[2][AR_MAX_RANKS];  // combines after each push
   const int P = p.P;
   const int tid = threadIdx.x;
   for (int r = tid; r < P; r += kThreads) {
@@ -106,9 +107,15 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     }
     __syncthreads();
     if (tid < 2) {  // leaf order = the program's pushes in order
-      int j = 0;
-      for (int i = 0; i < p.prog_len; ++i)
-        if (s_prog[tid][i] >= 0) s_push[tid][j++] = s_prog[tid][i];
+      int j = -1;
+      for (int i = 0; i < p.prog_len; ++i) {
+        if (s_prog[tid][i] >= 0) {
+          s_push[tid][++j] = s_prog[tid][i];
+          s_ncomb[tid][j] = 0;
+        } else {
+          ++s_ncomb[tid][j];
+        }
+      }
     }
   }
   __syncthreads();
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
   if (v > n || (v == n && p.tail == 0)) return;
   const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
   const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
-  const int16_t* ops = s_prog[t];
+  const int16_t* ncomb = s_ncomb[t];
   // rank of the k-th value in the push sequence
   auto rank_of = [&](int k) -> int {
     if constexpr (ALGO == kRing) {
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
       wr = wr + 1 == kSlots ? 0 : wr + 1;
       return widen<DT>(raw);
     };
-    acc = fold_sequence<DT, OP, ALGO>(P, ops, p.prog_len, next);
+    acc = fold_sequence<DT, OP, ALGO>(P, ncomb, next);
     cp_async_wait<0>();
     const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
     if constexpr (SCATTER) {
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     // the trailing partial vector: element-wise loads, same order
     int j = 0;
     auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[rank_of(j++)] + n, p.tail)); };
-    acc = fold_sequence<DT, OP, ALGO>(P, ops, p.prog_len, next);
+    acc = fold_sequence<DT, OP, ALGO>(P, ncomb, next);
     const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
     for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
   }

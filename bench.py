@@ -41,9 +41,13 @@ PROFILES = {
     "p8_64MiB_fp32_ring_ddp_mean": ("static_ring_p8_64MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p8_64MiB_bf16_tree": ("static_tree_p8_64MiB_bf16.ncu.txt", _STATIC + [_CSRC + "ar_static_bf16.cu"], 1.0),
     "p8_256MiB_bf16_tree": ("static_tree_p8_64MiB_bf16.ncu.txt", _STATIC + [_CSRC + "ar_static_bf16.cu"], 4.0),
-    "p72_4MiB_int32_sum_ring": ("staged_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
-    "p72_16MiB_int32_sum_ring": ("staged_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
+    "p72_4MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_16MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
+    "p72_4MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll.cu"], 1.0),
+    "p8_rs_8MiB_shards_fp32": ("pipelined_reduce_scatter_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
 
 WORKLOADS = {
@@ -62,6 +66,8 @@ WORKLOADS = {
                                dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
     "p72_4MiB_int32_sum_ring": dict(P=72, count=1024 * 1024, kind="int", sigma=1.0,
                                     dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
+    "p72_4MiB_int32_max_tree": dict(P=72, count=1024 * 1024, kind="int", sigma=1.0,
+                                    dtype="i32", op="max", algo="tree", scale=1.0, seed=0),
     "p8_4KiB_fp32_ll": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
                             algo="ll", scale=1.0, seed=0),
     # the ring's two halves as standalone collectives: count = elements per shard
