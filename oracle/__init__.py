@@ -92,6 +92,13 @@ class Oracle:
         L.oracle_all_gather.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), sz,
                                         ctypes.c_int]
         L.oracle_all_gather.restype = ctypes.c_int
+        L.oracle_allreduce_hier.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp),
+                                            ctypes.POINTER(vp), sz, sz, sz, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_float]
+        L.oracle_allreduce_hier.restype = ctypes.c_int
+        L.oracle_allreduce_hier_sampled.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, sz, sz,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
+        L.oracle_allreduce_hier_sampled.restype = ctypes.c_int
         self.lib = L
         self.path = path
 
@@ -129,6 +136,33 @@ class Oracle:
         out = np.zeros(m, dtype=NP_DTYPE[dtype])
         _check(self.lib.oracle_allreduce_sampled(P, vals.ctypes.data, idx.ctypes.data, m, count,
                                                  dtype, op, algo, scale, out.ctypes.data))
+        return out
+
+    def allreduce_hier(self, sends, group: int, dtype: int, op: int = SUM, scale: float = 1.0,
+                       begin: int = 0, end: int | None = None):
+        """Hierarchical all-reduce, groups of `group` consecutive ranks."""
+        P = len(sends)
+        count = int(sends[0].shape[0])
+        want = NP_DTYPE[dtype]
+        sends = [np.ascontiguousarray(s) for s in sends]
+        for s in sends:
+            if s.dtype != want or s.shape != (count,):
+                raise OracleError("all send arrays must share dtype and length")
+        recvs = [np.zeros(count, dtype=want) for _ in range(P)]
+        end = count if end is None else end
+        sp = (ctypes.c_void_p * P)(*[s.ctypes.data for s in sends])
+        rp = (ctypes.c_void_p * P)(*[r.ctypes.data for r in recvs])
+        _check(self.lib.oracle_allreduce_hier(P, group, sp, rp, count, begin, end, dtype, op, scale))
+        return recvs
+
+    def allreduce_hier_sampled(self, vals: np.ndarray, idx, count: int, group: int, dtype: int,
+                               op: int = SUM, scale: float = 1.0) -> np.ndarray:
+        vals = np.ascontiguousarray(vals, dtype=NP_DTYPE[dtype])
+        idx = np.ascontiguousarray(idx, dtype=np.uint64)
+        P, m = vals.shape
+        out = np.zeros(m, dtype=NP_DTYPE[dtype])
+        _check(self.lib.oracle_allreduce_hier_sampled(P, group, vals.ctypes.data, idx.ctypes.data, m,
+                                                      count, dtype, op, scale, out.ctypes.data))
         return out
 
     def reduce_scatter(self, sends, dtype: int, op: int = SUM, scale: float = 1.0):
@@ -206,6 +240,14 @@ def tree_expr(P: int, tree: int) -> str:
 
 def reduce_scatter(*a, **k):
     return default().reduce_scatter(*a, **k)
+
+
+def allreduce_hier(*a, **k):
+    return default().allreduce_hier(*a, **k)
+
+
+def allreduce_hier_sampled(*a, **k):
+    return default().allreduce_hier_sampled(*a, **k)
 
 
 def all_gather(*a, **k):

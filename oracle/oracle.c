@@ -47,6 +47,18 @@
  *   Min / max: acc = (x < acc) ? x : acc (min), acc = (x > acc) ? x : acc
  *   (max), in fold order; on ties the earlier operand is kept.
  *
+ *   HIERARCHICAL (lecture_068 page, section 06: intra-node reduce-scatter,
+ *   inter-node ring all-reduce, intra-node all-gather): P = G groups of Q
+ *   ranks, rank r = g*Q + q.  Phase 1 is a ring reduce-scatter inside each
+ *   group: the count is cut into Q chunks of L1 = roundup(ceil(count/Q), V)
+ *   elements and chunk c1 of group g is folded from local rank c1:
+ *       part_g = x_{g,c1} (+) x_{g,c1+1} (+) ... (+) x_{g,c1+Q-1}  (local mod Q).
+ *   Phase 2 is a ring all-reduce of chunk c1 across the G groups: the chunk's
+ *   len1 elements are cut into G sub-chunks of L2 = roundup(ceil(len1/G), V)
+ *   and an element of sub-chunk c2 is folded from group c2:
+ *       y = part_{c2} (+) part_{c2+1} (+) ... (+) part_{c2+G-1}   (groups mod G).
+ *   Phase 3 only copies.  G = 1 or Q = 1 reduce to the plain ring.
+ *
  *   REDUCE-SCATTER ("NCCL, NIXL, and Distributed GPU Communication", section
  *   "Reduce-scatter"): every rank holds P shards of recvcount elements; the
  *   shards are reduced across ranks and rank s receives reduced shard s.
@@ -339,5 +351,60 @@ int oracle_all_gather(int P, const void* const* send, void* const* recv, size_t 
             for (size_t i = 0; i < sendcount; ++i)
                 memcpy((char*)recv[r] + ((size_t)s * sendcount + i) * es,
                        (const char*)send[s] + i * es, es);
+    return 0;
+}
+
+/* Hierarchical fold of one element (see the header): x[r] = rank r's input. */
+static acc_t reduce_element_hier(const acc_t* x, int P, int Q, size_t count, size_t e, int dtype,
+                                 int op, float scale) {
+    int G = P / Q;
+    size_t V = vec_elems(dtype);
+    size_t L1 = round_up((count + (size_t)Q - 1) / (size_t)Q, V);
+    size_t c1 = e / L1;
+    size_t end1 = (c1 + 1) * L1 < count ? (c1 + 1) * L1 : count;
+    size_t len1 = end1 - c1 * L1;
+    size_t L2 = round_up((len1 + (size_t)G - 1) / (size_t)G, V);
+    size_t c2 = (e - c1 * L1) / L2;
+    acc_t total = {0};
+    for (int j = 0; j < G; ++j) {
+        int g = (int)((c2 + (size_t)j) % (size_t)G);
+        acc_t part = x[g * Q + (int)(c1 % (size_t)Q)];
+        for (int k = 1; k < Q; ++k) part = combine(part, x[g * Q + (int)((c1 + (size_t)k) % (size_t)Q)], dtype, op);
+        total = j == 0 ? part : combine(total, part, dtype, op);
+    }
+    if (dtype != OR_I32 && scale != 1.0f) total.f = total.f * scale;
+    return total;
+}
+
+/*
+ * Hierarchical all-reduce with groups of Q ranks (Q must divide P), output
+ * elements [begin, end) to every rank.  Returns 0, -1 invalid, -2 bad scale.
+ */
+int oracle_allreduce_hier(int P, int Q, const void* const* send, void* const* recv, size_t count,
+                          size_t begin, size_t end, int dtype, int op, float scale) {
+    int rc = check_args(P, dtype, op, OR_ALGO_RING, scale);
+    if (rc) return rc;
+    if (Q < 1 || Q > P || P % Q != 0 || begin > end || end > count) return -1;
+    acc_t x[OR_MAX_RANKS];
+    for (size_t e = begin; e < end; ++e) {
+        for (int r = 0; r < P; ++r) x[r] = load_widened(send[r], e, dtype);
+        acc_t y = reduce_element_hier(x, P, Q, count, e, dtype, op, scale);
+        for (int r = 0; r < P; ++r) store_narrowed(recv[r], e, y, dtype);
+    }
+    return 0;
+}
+
+/* Sampled form of oracle_allreduce_hier (layout as oracle_allreduce_sampled). */
+int oracle_allreduce_hier_sampled(int P, int Q, const void* vals, const size_t* idx, size_t m,
+                                  size_t count, int dtype, int op, float scale, void* out) {
+    int rc = check_args(P, dtype, op, OR_ALGO_RING, scale);
+    if (rc) return rc;
+    if (Q < 1 || Q > P || P % Q != 0) return -1;
+    acc_t x[OR_MAX_RANKS];
+    for (size_t i = 0; i < m; ++i) {
+        if (idx[i] >= count) return -1;
+        for (int r = 0; r < P; ++r) x[r] = load_widened(vals, (size_t)r * m + i, dtype);
+        store_narrowed(out, i, reduce_element_hier(x, P, Q, count, idx[i], dtype, op, scale), dtype);
+    }
     return 0;
 }

@@ -128,7 +128,7 @@ def assert_bitwise(a: np.ndarray, b: np.ndarray, what: str):
 
 # ------------------------------------------------------------ ring by steps
 
-def ring_message_passing(sends, dtype: int, op: int, scale: float):
+def ring_message_passing(sends, dtype: int, op: int, scale: float, widened_input: bool = False):
     """The ring all-reduce run literally: chunks travel between P buffers.
 
     Reduce-scatter: at step s (0 .. P-2) rank r sends its partial of chunk
@@ -137,12 +137,13 @@ def ring_message_passing(sends, dtype: int, op: int, scale: float):
     and narrowing.  All-gather: at step s rank r forwards chunk (r + 1 - s)
     mod P to rank r+1, which stores it.  Chunks are P equal pieces whose
     length is rounded up to a 16-byte multiple (trailing pieces may be empty).
+    With widened_input the P inputs are already accumulator values (lists).
     """
     P = len(sends)
     count = len(sends[0])
     L = ceil_div(ceil_div(count, P), VEC[dtype]) * VEC[dtype]
     bounds = [(min(count, c * L), min(count, (c + 1) * L)) for c in range(P)]
-    buf = [widened(s, dtype) for s in sends]
+    buf = [list(s) if widened_input else widened(s, dtype) for s in sends]
     for s in range(P - 1):
         msgs = []
         for r in range(P):
@@ -589,8 +590,101 @@ def pin_collectives_order_independent(O):
             assert_bitwise(gathered[r], np.concatenate([x[:rc] for x in sends]), f"AG P={P} rank={r}")
 
 
+# ------------------------------------------------------------ hierarchical
+
+def hierarchical_steps(sends, Q: int, dtype: int, op: int, scale: float):
+    """The hierarchical all-reduce run phase by phase on P buffers (lecture_068
+    page, section 06): a ring reduce-scatter inside every group of Q ranks,
+    then, for each intra-group chunk, a ring all-reduce of the G holders'
+    partials (the step-by-step ring of ring_message_passing, on that chunk),
+    then the all-gather copies."""
+    P = len(sends)
+    G = P // Q
+    count = len(sends[0])
+    V = VEC[dtype]
+    L1 = ceil_div(ceil_div(count, Q), V) * V
+    # phase 1: within each group, chunk c1 folded from local rank c1 (ring RS)
+    parts = []   # parts[g] = list of per-element partials (Python scalars)
+    for g in range(G):
+        xs = [widened(sends[g * Q + q], dtype) for q in range(Q)]
+        part = [None] * count
+        for c1 in range(Q):
+            lo, hi = min(count, c1 * L1), min(count, (c1 + 1) * L1)
+            for e in range(lo, hi):
+                acc = xs[c1][e]
+                for k in range(1, Q):
+                    acc = combine(acc, xs[(c1 + k) % Q][e], dtype, op)
+                part[e] = acc
+        parts.append(part)
+    # phase 2: per chunk c1, the literal ring all-reduce over the G partials
+    out = np.zeros(count, dtype=NP_DTYPE[dtype])
+    for c1 in range(Q):
+        lo, hi = min(count, c1 * L1), min(count, (c1 + 1) * L1)
+        if hi <= lo:
+            continue
+        chunk = [parts[g][lo:hi] for g in range(G)]
+        red = ring_message_passing(chunk, dtype, op, scale, widened_input=True)
+        out[lo:hi] = red[0]
+    return [out.copy() for _ in range(P)]
+
+
+def pin_hierarchical_steps(O, quick: bool = False):
+    rng = np.random.default_rng(61)
+    cases = [(4, 2), (6, 3), (6, 2), (8, 4), (9, 3), (8, 2), (12, 4)] if not quick else [(9, 3), (12, 4)]
+    for P, Q in cases:
+        for count in ((1, 7, 33, 80) if not quick else (33,)):
+            for dtype in (F32, BF16, I32):
+                sends = random_inputs(rng, P, count, dtype)
+                for op in (SUM, MIN, MAX):
+                    scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                    for scale in scales:
+                        want = hierarchical_steps(sends, Q, dtype, op, scale)
+                        got = O.allreduce_hier(sends, Q, dtype, op, scale)
+                        for r in (0, P - 1):
+                            assert_bitwise(got[r], want[r], f"hier P={P} Q={Q} count={count} "
+                                                            f"dtype={dtype} op={op} scale={scale}")
+
+
+def pin_hierarchical_degenerate_is_ring(O):
+    """One group (G = 1) or groups of one rank (Q = 1): the hierarchy collapses
+    to the plain ring, order for order."""
+    rng = np.random.default_rng(67)
+    for P in (1, 2, 5, 8, 12):
+        for count in (3, 64, 1001):
+            for dtype in (F32, BF16):
+                sends = random_inputs(rng, P, count, dtype)
+                ring = O.allreduce(sends, dtype, SUM, RING)[0]
+                assert_bitwise(O.allreduce_hier(sends, P, dtype, SUM)[0], ring, f"G=1 P={P} count={count}")
+                assert_bitwise(O.allreduce_hier(sends, 1, dtype, SUM)[0], ring, f"Q=1 P={P} count={count}")
+    # and it is a different order in general (so the grouping is applied)
+    sends = random_inputs(rng, 8, 4096, F32)
+    assert not np.array_equal(O.allreduce_hier(sends, 4, F32, SUM)[0], O.allreduce(sends, F32, SUM, RING)[0])
+
+
+def pin_hierarchical_order_independent(O):
+    rng = np.random.default_rng(71)
+    for P, Q in ((72, 8), (72, 9), (16, 4)):
+        sends = random_inputs(rng, P, 257, I32)
+        wide = np.stack([x.astype(np.int64) for x in sends])
+        tot = wide.sum(axis=0) & 0xFFFFFFFF
+        tot = np.where(tot >= 2 ** 31, tot - 2 ** 32, tot).astype(np.int32)
+        assert_bitwise(O.allreduce_hier(sends, Q, I32, SUM)[0], tot, f"hier int sum P={P}")
+        assert_bitwise(O.allreduce_hier(sends, Q, I32, MIN)[0], wide.min(axis=0).astype(np.int32),
+                       f"hier int min P={P}")
+        vals = np.stack(random_inputs(rng, P, 257, F32))
+        got = O.allreduce_hier(list(vals), Q, F32, MAX)[0]
+        assert_bitwise(got, vals.max(axis=0), f"hier f32 max P={P}")
+        idx = np.array([0, 5, 100, 256], dtype=np.uint64)
+        fsend = random_inputs(rng, P, 257, F32)
+        full = O.allreduce_hier(fsend, Q, F32, SUM, 0.5)[0]
+        samp = O.allreduce_hier_sampled(np.stack([x[idx.astype(np.int64)] for x in fsend]), idx, 257, Q,
+                                        F32, SUM, 0.5)
+        assert_bitwise(samp, full[idx.astype(np.int64)], f"hier sampled P={P}")
+
+
 ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_tree_expressions,
             pin_tree_structure, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
             pin_sampled_matches_full, pin_reduce_scatter_worked_example, pin_all_gather_worked_example,
             pin_allreduce_is_reduce_scatter_then_all_gather, pin_reduce_scatter_ring_steps,
-            pin_collectives_order_independent]
+            pin_collectives_order_independent, pin_hierarchical_steps,
+            pin_hierarchical_degenerate_is_ring, pin_hierarchical_order_independent]

@@ -42,14 +42,20 @@ MUTANTS = {
                       "if (lower >= 0x8000u) upper += 1;"),
     "scale_dropped": ("    if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;\n    return acc;",
                       "    return acc;"),
-    "only_rank0_written": ("for (int r = 0; r < P; ++r) store_narrowed(recv[r], e, y, dtype);",
-                           "store_narrowed(recv[0], e, y, dtype);"),
+    "only_rank0_written": ("algo, scale);\n        for (int r = 0; r < P; ++r) store_narrowed(recv[r], e, y, dtype);",
+                           "algo, scale);\n        store_narrowed(recv[0], e, y, dtype);"),
     "bf16_widen_shift": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
     "rs_shard_start": ("            acc_t acc = x[s];\n            for (int k = 1; k < P; ++k) acc = combine(acc, x[(s + k) % P], dtype, op);",
                        "            acc_t acc = x[(s + 1) % P];\n            for (int k = 2; k <= P; ++k) acc = combine(acc, x[(s + k) % P], dtype, op);"),
     "rs_wrong_shard": ("            size_t e = (size_t)s * recvcount + i;", "            size_t e = (size_t)((s + 1) % P) * recvcount + i;"),
     "rs_scale_dropped": ("            if (dtype != OR_I32 && scale != 1.0f) acc.f = acc.f * scale;\n            store_narrowed(recv[s], i, acc, dtype);",
                          "            store_narrowed(recv[s], i, acc, dtype);"),
+    "hier_group_start": ("        int g = (int)((c2 + (size_t)j) % (size_t)G);",
+                         "        int g = (int)((c2 + (size_t)j + 1) % (size_t)G);"),
+    "hier_local_start": ("        acc_t part = x[g * Q + (int)(c1 % (size_t)Q)];",
+                         "        acc_t part = x[g * Q];"),
+    "hier_subchunk_len": ("    size_t L2 = round_up((len1 + (size_t)G - 1) / (size_t)G, V);",
+                          "    size_t L2 = round_up((count + (size_t)G - 1) / (size_t)G, V);"),
     "ag_wrong_offset": ("memcpy((char*)recv[r] + ((size_t)s * sendcount + i) * es,",
                         "memcpy((char*)recv[r] + ((size_t)((s + r) % P) * sendcount + i) * es,"),
 }
@@ -67,7 +73,7 @@ def test_mutant_is_caught(name, tmp_path):
     failures = []
     for pin in pins.ALL_PINS:
         try:
-            if pin is pins.pin_ring_simulation:
+            if pin in (pins.pin_ring_simulation, pins.pin_hierarchical_steps):
                 pin(O, quick=True)
             else:
                 pin(O)
