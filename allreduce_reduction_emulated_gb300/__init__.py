@@ -27,13 +27,14 @@ AR_SUCCESS, AR_ERR_INVALID_ARG, AR_ERR_CUDA, AR_ERR_UNSUPPORTED, AR_ERR_TIMEOUT,
 # ar_dtype_t, ar_op_t, ar_algo_t, ar_option_t
 AR_FLOAT32, AR_BFLOAT16, AR_INT32 = 0, 1, 2
 AR_SUM, AR_MIN, AR_MAX = 0, 1, 2
-AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL = 0, 1, 2, 3
-AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER = 0, 1, 2, 3
+AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL, AR_ALGO_HIER = 0, 1, 2, 3, 4
+AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER, AR_OPT_HIER_GROUP = range(5)
 AR_MAX_RANKS = 256
 AR_NOALLOC_MAX_RANKS, AR_NOALLOC_MAX_BYTES = 8, 65536
 
 OPS = {"sum": AR_SUM, "min": AR_MIN, "max": AR_MAX}
-ALGOS = {"auto": AR_ALGO_AUTO, "ring": AR_ALGO_RING, "tree": AR_ALGO_TREE, "ll": AR_ALGO_LL}
+ALGOS = {"auto": AR_ALGO_AUTO, "ring": AR_ALGO_RING, "tree": AR_ALGO_TREE, "ll": AR_ALGO_LL,
+         "hier": AR_ALGO_HIER}
 
 
 class ArError(RuntimeError):

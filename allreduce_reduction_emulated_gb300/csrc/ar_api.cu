@@ -28,6 +28,7 @@ struct ar_comm {
   int* status = nullptr;         // device ar_status_t word
   int16_t* tree_prog = nullptr;  // device: tree 0 program then tree 1 program
   int prog_len = 0;
+  int hier_group = 8;            // AR_ALGO_HIER: ranks per group
 };
 
 namespace {
@@ -47,7 +48,8 @@ long long env_ll(const char* name, long long dflt) {
 bool valid_dtype(int d) { return d == AR_FLOAT32 || d == AR_BFLOAT16 || d == AR_INT32; }
 bool valid_op(int o) { return o == AR_SUM || o == AR_MIN || o == AR_MAX; }
 bool valid_algo(int a) {
-  return a == AR_ALGO_AUTO || a == AR_ALGO_RING || a == AR_ALGO_TREE || a == AR_ALGO_LL;
+  return a == AR_ALGO_AUTO || a == AR_ALGO_RING || a == AR_ALGO_TREE || a == AR_ALGO_LL ||
+         a == AR_ALGO_HIER;
 }
 
 // Postorder program of tree t: push own rank, then each child's subtree
@@ -77,7 +79,11 @@ int program_depth(const std::vector<int16_t>& prog) {
 const char* dtype_name(int d) { return d == AR_FLOAT32 ? "f32" : d == AR_BFLOAT16 ? "bf16" : "i32"; }
 const char* op_name(int o) { return o == AR_SUM ? "sum" : o == AR_MIN ? "min" : "max"; }
 const char* algo_name(int a) {
-  return a == AR_ALGO_RING ? "ring" : a == AR_ALGO_TREE ? "tree" : a == AR_ALGO_LL ? "ll" : "auto";
+  return a == AR_ALGO_RING   ? "ring"
+         : a == AR_ALGO_TREE ? "tree"
+         : a == AR_ALGO_LL   ? "ll"
+         : a == AR_ALGO_HIER ? "hier"
+                             : "auto";
 }
 
 void release(ar_comm* c) {
@@ -183,6 +189,7 @@ ar::Call base_call(ar_comm_t c, void* stream) {
   call.skip_produce = c->skip_produce;
   call.epoch = 0;
   call.shard = 0;
+  call.group = c->hier_group;
   call.algo = ar::kRing;
   call.scale = 1.0f;
   call.op = AR_SUM;
@@ -294,6 +301,10 @@ ar_status_t ar_set_option(ar_comm_t c, ar_option_t option, long long value) {
     case AR_OPT_LL_SKIP_PRODUCER:
       c->skip_produce = value != 0;
       return AR_SUCCESS;
+    case AR_OPT_HIER_GROUP:
+      if (value < 1 || value > c->P || c->P % value != 0) return AR_ERR_INVALID_ARG;
+      c->hier_group = (int)value;
+      return AR_SUCCESS;
     default:
       return AR_ERR_INVALID_ARG;
   }
@@ -324,6 +335,7 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
 
   ar_algo_t chosen = resolve(c, count, dtype, algo);
   if (chosen == AR_ALGO_LL && count * esize > c->ll_max_bytes) return AR_ERR_UNSUPPORTED;
+  if (chosen == AR_ALGO_HIER && P % c->hier_group != 0) return AR_ERR_UNSUPPORTED;
   if (chosen == AR_ALGO_LL) {
     // The LL epoch is a launch parameter: a captured launch would replay one
     // epoch forever and could accept a previous replay's staged words.  Under
@@ -347,7 +359,8 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   call.count = count;
   call.dtype = dtype;
   call.op = op;
-  call.algo = chosen == AR_ALGO_TREE ? ar::kTree : ar::kRing;
+  call.algo = chosen == AR_ALGO_TREE ? ar::kTree : chosen == AR_ALGO_HIER ? ar::kHier : ar::kRing;
+  call.group = c->hier_group;
   call.scale = scale;
   call.stream = static_cast<cudaStream_t>(stream);
   call.sms = c->sms;
@@ -376,6 +389,8 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
     }
     call.epoch = ++c->epoch;
     e = ar::launch_ll(call, &info);
+  } else if (chosen == AR_ALGO_HIER) {
+    e = ar::launch_generic(call, &info);
   } else if (P <= ar::kMaxStaticRanks) {
     e = dtype == AR_FLOAT32    ? ar::launch_static_f32(call, &info)
         : dtype == AR_BFLOAT16 ? ar::launch_static_bf16(call, &info)

@@ -11,7 +11,7 @@ namespace ar {
 
 enum : int { kF32 = 0, kBF16 = 1, kI32 = 2 };
 enum : int { kSum = 0, kMin = 1, kMax = 2 };
-enum : int { kRing = 1, kTree = 2 };
+enum : int { kRing = 1, kTree = 2, kHier = 4 };
 
 // A 16-byte vector of each data type and the type it is accumulated in:
 // fp32 and bf16 accumulate in fp32, int32 in int32 with wrap-around adds.

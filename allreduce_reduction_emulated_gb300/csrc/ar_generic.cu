@@ -40,6 +40,8 @@ struct GenericParams {
   const int16_t* prog;  // device: tree 0 program then tree 1 program (prog_len ops each)
   int prog_len;
   int P;
+  int Q;                // hierarchical: ranks per group (P = G * Q)
+  uint64_t count;       // elements per rank (hierarchical sub-chunk lengths)
   uint64_t nfull;
   uint64_t split;  // ring: vectors per chunk; tree: first vector of tree 1
   float scale;
@@ -59,12 +61,22 @@ __device__ __forceinline__ void cp_async_wait() {
 // Folds the column in the algorithm's order; next() yields the widened
 // input of the next rank in the push sequence.  The tree runs as P pushes,
 // push j followed by ncomb[j] combines (the postorder program regrouped).
+// The hierarchical order folds each group's Q values, then the G partials.
 template <int DT, int OP, int ALGO, class Next>
-__device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ncomb, Next& next) {
+__device__ __forceinline__ Acc<DT> fold_sequence(int P, int Q, const int16_t* ncomb, Next& next) {
   if constexpr (ALGO == kRing) {
     Acc<DT> acc = next();
     for (int k = 1; k < P; ++k) fold<DT, OP>(acc, next());
     return acc;
+  } else if constexpr (ALGO == kHier) {
+    Acc<DT> total;
+    for (int j = 0; j < P; j += Q) {
+      Acc<DT> part = next();
+      for (int i = 1; i < Q; ++i) fold<DT, OP>(part, next());
+      if (j == 0) total = part;
+      else fold<DT, OP>(total, part);
+    }
+    return total;
   } else {
     // the stack's top entry lives in registers; only deeper entries go to
     // the (local-memory) array: a push stores the old top, a combine loads
@@ -84,6 +96,28 @@ __device__ __forceinline__ Acc<DT> fold_sequence(int P, const int16_t* ncomb, Ne
     return top;
   }
 }
+
+// The ranks of a column in push order, one at a time.
+template <int ALGO>
+struct RankCursor {
+  int a, b;               // ring: rank; tree: index; hier: local index, group index
+  int P, Q, G, a0, b0;    // hier: start local index a0 (chunk c1 mod Q), group b0 (c2)
+  const int16_t* push;    // tree leaf order
+  __device__ __forceinline__ int next() {
+    if constexpr (ALGO == kRing) {
+      const int r = a;
+      a = a + 1 == P ? 0 : a + 1;
+      return r;
+    } else if constexpr (ALGO == kTree) {
+      return push[a++];
+    } else {
+      const int r = b * Q + a;
+      a = a + 1 == Q ? 0 : a + 1;
+      if (a == a0) b = b + 1 == G ? 0 : b + 1;   // a group's Q ranks are done
+      return r;
+    }
+  }
+};
 
 // SCATTER (ring only): reduce-scatter -- chunk c is shard c and its result
 // goes only to rank c's receive buffer, at the shard-relative position.
@@ -126,15 +160,28 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
   const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
   const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
   const int16_t* ncomb = s_ncomb[t];
-  // rank of the k-th value in the push sequence
-  auto rank_of = [&](int k) -> int {
-    if constexpr (ALGO == kRing) {
-      int r = first + k;
-      return r >= P ? r - P : r;
-    } else {
-      return s_push[t][k];
-    }
-  };
+  RankCursor<ALGO> cur;
+  cur.P = P;
+  cur.push = s_push[t];
+  if constexpr (ALGO == kRing) {
+    cur.a = first;
+  } else if constexpr (ALGO == kTree) {
+    cur.a = 0;
+  } else {
+    // hierarchical: intra-group chunk c1 (split = its length in vectors), then
+    // sub-chunk c2 of that chunk across the G groups
+    const uint64_t V = 16 / Lanes<DT>::kBytes;
+    const uint64_t c1 = v / p.split;
+    const uint64_t lo = c1 * p.split * V;
+    const uint64_t hi = lo + p.split * V < p.count ? lo + p.split * V : p.count;
+    const int G = P / p.Q;
+    const uint64_t L2v = ((hi - lo + G - 1) / G + V - 1) / V;
+    const uint64_t c2 = (v - c1 * p.split) / L2v;
+    cur.Q = p.Q;
+    cur.G = G;
+    cur.a0 = cur.a = (int)(c1 % (uint64_t)p.Q);
+    cur.b0 = cur.b = (int)c2;
+  }
 
   Acc<DT> acc;
   if (v < n) {
@@ -142,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     constexpr uint32_t kSlotStride = kThreads * 16;
 #pragma unroll
     for (int k = 0; k < kWindow; ++k) {
-      if (k < P) cp_async16(base + k * kSlotStride, s_send[rank_of(k)] + v);
+      if (k < P) cp_async16(base + k * kSlotStride, s_send[cur.next()] + v);
       cp_async_commit();
     }
     int j = 0;          // values consumed
@@ -152,14 +199,14 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
       cp_async_wait<kWindow - 1>();  // value j has landed
       const uint4 raw = slots[rd][tid];
       const int k = j + kWindow;
-      if (k < P) cp_async16(base + wr * kSlotStride, s_send[rank_of(k)] + v);
+      if (k < P) cp_async16(base + wr * kSlotStride, s_send[cur.next()] + v);
       cp_async_commit();
       ++j;
       rd = rd + 1 == kSlots ? 0 : rd + 1;
       wr = wr + 1 == kSlots ? 0 : wr + 1;
       return widen<DT>(raw);
     };
-    acc = fold_sequence<DT, OP, ALGO>(P, ncomb, next);
+    acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
     cp_async_wait<0>();
     const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
     if constexpr (SCATTER) {
@@ -169,9 +216,8 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     }
   } else {
     // the trailing partial vector: element-wise loads, same order
-    int j = 0;
-    auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[rank_of(j++)] + n, p.tail)); };
-    acc = fold_sequence<DT, OP, ALGO>(P, ncomb, next);
+    auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[cur.next()] + n, p.tail)); };
+    acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
     const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
     for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
   }
@@ -188,10 +234,15 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
   p.prog = c.tree_prog;
   p.prog_len = c.prog_len;
   p.P = c.P;
+  p.Q = c.group;
+  p.count = c.count;
   const uint64_t V = (uint64_t)vec_elems(DT);
   p.nfull = c.count / V;
   p.tail = (int)(c.count % V);
-  p.split = ALGO == kRing ? ring_chunk_vectors(c.count, c.P, DT) : tree_split_vectors(c.count, DT);
+  if (ALGO == kHier && (c.group < 1 || c.P % c.group != 0)) return cudaErrorInvalidValue;
+  p.split = ALGO == kRing   ? ring_chunk_vectors(c.count, c.P, DT)
+            : ALGO == kHier ? ring_chunk_vectors(c.count, c.group, DT)  // intra-group chunk
+                            : tree_split_vectors(c.count, DT);
   p.scale = c.scale;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   if (ALGO == kTree && c.prog_len > kMaxProg) return cudaErrorInvalidValue;
@@ -199,7 +250,7 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
   const uint64_t grid = (columns + kThreads - 1) / kThreads;
   if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(p);
-  info->kernel = ALGO == kRing ? "pipelined_ring" : "pipelined_tree";
+  info->kernel = ALGO == kRing ? "pipelined_ring" : ALGO == kHier ? "pipelined_hier" : "pipelined_tree";
   info->grid = (int)grid;
   info->block = kThreads;
   info->smem = sizeof(uint4) * kSlots * kThreads;
@@ -210,6 +261,7 @@ template <int DT, int OP>
 cudaError_t launch_generic_algo(const Call& c, LaunchInfo* info) {
   if (c.algo == kRing) return launch_generic_one<DT, OP, kRing>(c, info);
   if (c.algo == kTree) return launch_generic_one<DT, OP, kTree>(c, info);
+  if (c.algo == kHier) return launch_generic_one<DT, OP, kHier>(c, info);
   return cudaErrorInvalidValue;
 }
 
@@ -234,6 +286,8 @@ cudaError_t launch_scatter_one(const Call& c, LaunchInfo* info) {
   p.prog = nullptr;
   p.prog_len = 0;
   p.P = c.P;
+  p.Q = c.P;
+  p.count = c.count;
   const uint64_t V = (uint64_t)vec_elems(DT);
   if (c.shard % V != 0) return cudaErrorInvalidValue;  // whole vectors per shard only
   p.nfull = c.count / V;

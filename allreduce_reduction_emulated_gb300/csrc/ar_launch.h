@@ -33,6 +33,7 @@ struct Call {
   // reduce-scatter / all-gather: elements per shard (recvcount / sendcount);
   // count is then the length of the larger buffers (P * shard)
   size_t shard;
+  int group;                    // hierarchical order: ranks per group
   uint32_t epoch;
   uint32_t spin_limit;
   int skip_produce;

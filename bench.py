@@ -61,6 +61,10 @@ WORKLOADS = {
                                      dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
     "p72_16MiB_int32_max_tree": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
                                      dtype="i32", op="max", algo="tree", scale=1.0, seed=0),
+    "p72_16MiB_int32_sum_hier": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
+                                     dtype="i32", op="sum", algo="hier", scale=1.0, seed=0, group=8),
+    "p72_16MiB_fp32_sum_hier": dict(P=72, count=4 * 1024 * 1024, kind="normal", sigma=1e-3,
+                                    dtype="f32", op="sum", algo="hier", scale=1.0 / 72, seed=3, group=8),
     # smaller cases of the same kernels, sized for profiler captures (inputs still exceed L2)
     "p8_64MiB_bf16_tree": dict(P=8, count=32 * 1024 * 1024, kind="normal_bf16", sigma=1e-2,
                                dtype="bf16", op="sum", algo="tree", scale=1.0, seed=0),
@@ -257,9 +261,9 @@ def oracle_throughput(w: dict, host_sends, seconds: float):
     coll = w.get("coll", "allreduce")
     dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
     op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
-    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL}[w["algo"]]
+    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL, "hier": None}[w["algo"]]
     nccl_bytes = sizes_of(w)[2]
-    if coll == "allreduce":
+    if coll == "allreduce" and algo is not None:
         recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
         oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, min(count, 65536), recvs)  # warm
     done, t0 = 0, time.perf_counter()
@@ -268,6 +272,8 @@ def oracle_throughput(w: dict, host_sends, seconds: float):
             oracle.reduce_scatter(host_sends, dt, op, w["scale"])
         elif coll == "all_gather":
             oracle.all_gather(host_sends, dt)
+        elif algo is None:
+            oracle.allreduce_hier(host_sends, w["group"], dt, op, w["scale"])
         else:
             oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, count, recvs)
         done += 1
@@ -287,8 +293,8 @@ def reference_arm(args, w, name):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    if w.get("coll", "allreduce") != "allreduce":
-        raise SystemExit("--impl reference times the all-reduce workloads")
+    if w.get("coll", "allreduce") != "allreduce" or w["algo"] == "hier":
+        raise SystemExit("--impl reference times the ring / tree / LL all-reduce workloads")
     P, count = w["P"], w["count"]
     dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
     op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
@@ -369,6 +375,8 @@ def ours_arm(args, w, name):
     sends = [synthetic.values_torch(w["kind"], w["seed"], r, 0, n_in, dev, w["sigma"]) for r in range(P)]
     recvs = [torch.empty(n_out, dtype=sends[0].dtype, device=dev) for _ in range(P)]
     comm = ar.ar_init(P)
+    if "group" in w:
+        ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, w["group"])
     stream = torch.cuda.current_stream()
 
     def call(xs, ys, s):

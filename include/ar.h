@@ -33,6 +33,16 @@
  *     atomic write): each rank's 4-byte payload words are staged as 8-byte
  *     {payload, flag = per-call epoch} words, reducers poll the flags (bounded
  *     spin) and fold in the RING order, so LL == RING bit for bit.
+ *   AR_ALGO_HIER -- the hierarchical all-reduce (lecture_068 page, section 06:
+ *     reduce-scatter inside each node, ring all-reduce between nodes,
+ *     all-gather inside each node) for P = G groups of Q consecutive ranks
+ *     (Q set by AR_OPT_HIER_GROUP, default 8).  Element e of intra-group
+ *     chunk c1 (Q chunks of L1 = roundup(ceil(count/Q), V)) is folded inside
+ *     each group g from local rank c1: part_g = x_{g,c1} (+) ... (+)
+ *     x_{g,c1+Q-1}; the G partials of chunk c1 (len1 elements, cut into G
+ *     sub-chunks of roundup(ceil(len1/G), V)) are then folded from group c2,
+ *     e's sub-chunk: part_{c2} (+) ... (+) part_{c2+G-1}.  G = 1 or Q = 1 is
+ *     the plain ring.  Never chosen by AUTO.
  *   AR_ALGO_AUTO -- LL when count * sizeof(element) <= the LL limit (64 KiB by
  *     default), RING above it (NCCL picks tree for small and ring for large
  *     messages by itself: "NCCL and NVSHMEM ...", the ring / tree paragraph).
@@ -71,7 +81,13 @@ typedef enum {
 
 typedef enum { AR_FLOAT32 = 0, AR_BFLOAT16 = 1, AR_INT32 = 2 } ar_dtype_t;
 typedef enum { AR_SUM = 0, AR_MIN = 1, AR_MAX = 2 } ar_op_t;
-typedef enum { AR_ALGO_AUTO = 0, AR_ALGO_RING = 1, AR_ALGO_TREE = 2, AR_ALGO_LL = 3 } ar_algo_t;
+typedef enum {
+    AR_ALGO_AUTO = 0,
+    AR_ALGO_RING = 1,
+    AR_ALGO_TREE = 2,
+    AR_ALGO_LL = 3,
+    AR_ALGO_HIER = 4
+} ar_algo_t;
 
 /* Largest number of emulated ranks one communicator takes. */
 #define AR_MAX_RANKS 256
@@ -147,8 +163,11 @@ typedef enum {
                                     at ar_init (default 65536 or AR_LL_MAX_BYTES)       */
     AR_OPT_LL_SPIN_LIMIT = 1,    /* polls of one flag before AR_ERR_TIMEOUT (>= 1)     */
     AR_OPT_DEBUG = 2,            /* nonzero: one line per call on stderr               */
-    AR_OPT_LL_SKIP_PRODUCER = 3  /* test hook: LL kernels skip staging, so every flag
+    AR_OPT_LL_SKIP_PRODUCER = 3, /* test hook: LL kernels skip staging, so every flag
                                     wait runs out and reports AR_ERR_TIMEOUT           */
+    AR_OPT_HIER_GROUP = 4        /* AR_ALGO_HIER ranks per group: a divisor of P
+                                    (default 8; a call whose P it does not divide
+                                    returns AR_ERR_UNSUPPORTED)                       */
 } ar_option_t;
 
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
