@@ -1,0 +1,72 @@
+"""Bucketed gradient all-reduce overlapped with the backward pass.
+
+DDP's pattern ("NCCL, NIXL, and Distributed GPU Communication", the DDP
+paragraph under "All-reduce" and the "Performance engineer checklist"): as
+soon as a bucket's gradients are ready, its all-reduce is enqueued on a
+separate communication stream, so later layers' backward compute overlaps
+earlier buckets' communication; total time ~ max(compute, comm) + a tail.
+
+Here every emulated rank's gradients live in one flat buffer (parameters in
+the order the backward produces them), cut into fixed-size buckets.  The
+producer reports how far the flat gradient is complete (an element offset
+and an event recorded after the writes); every bucket wholly below that
+offset is all-reduced on the communication stream after waiting on the
+event.  Plumbing only: the reduction is ar_allreduce.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import AR_ALGO_RING, AR_SUM, ar_allreduce, dtype_of
+
+
+class BucketReducer:
+    """All-reduces fixed-size buckets of P flat gradient buffers as they fill.
+
+    grads     P contiguous CUDA tensors of the same length (one per rank)
+    bucket    elements per bucket (the last one may be shorter)
+    comm      an ar_init communicator for P ranks
+    out       optional P result tensors (default: reduce in place)
+    """
+
+    def __init__(self, comm: int, grads, bucket: int, scale: float = 1.0, algo: int = AR_ALGO_RING,
+                 out=None, stream: torch.cuda.Stream | None = None):
+        self.comm = comm
+        self.grads = list(grads)
+        self.out = list(out) if out is not None else self.grads
+        self.total = self.grads[0].numel()
+        self.bucket = bucket
+        self.scale = scale
+        self.algo = algo
+        self.dtype = dtype_of(self.grads[0])
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        self.starts = list(range(0, self.total, bucket))
+        self.next_bucket = 0
+
+    def reset(self):
+        self.next_bucket = 0
+
+    def ready(self, upto: int, event: torch.cuda.Event) -> int:
+        """Elements [0, upto) are written once `event` completes: enqueue every
+        bucket that now lies wholly below upto.  Returns how many it enqueued."""
+        n = 0
+        while self.next_bucket < len(self.starts):
+            s = self.starts[self.next_bucket]
+            e = min(s + self.bucket, self.total)
+            if e > upto:
+                break
+            if n == 0:
+                self.stream.wait_event(event)
+            ar_allreduce(self.comm, [g[s:e] for g in self.grads], [o[s:e] for o in self.out], e - s,
+                         self.dtype, AR_SUM, self.algo, self.scale, self.stream)
+            self.next_bucket += 1
+            n += 1
+        return n
+
+    def finish(self) -> torch.cuda.Event:
+        """An event on the communication stream after the last bucket."""
+        if self.next_bucket != len(self.starts):
+            raise RuntimeError("BucketReducer.finish: not every bucket was reported ready")
+        ev = torch.cuda.Event()
+        ev.record(self.stream)
+        return ev

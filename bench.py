@@ -112,6 +112,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ddp-buckets", action="store_true",
                     help="DDP-style run: P=8 x 1,207,959,552 fp32 gradients in 185 x 25 MiB buckets per step")
+    ap.add_argument("--ddp-overlap", action="store_true",
+                    help="DDP backward (synthetic per-rank weight-gradient GEMMs) overlapped with the "
+                         "bucketed all-reduce: compute, comm, serial and overlapped step times")
+    ap.add_argument("--tokens", type=int, default=512,
+                    help="tokens per rank for --ddp-overlap's gradient GEMMs")
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep (P=8 fp32, 8 B .. 1 GiB per rank) with an alpha-beta fit")
     return ap.parse_args()
@@ -706,8 +711,111 @@ def ddp_buckets(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ DDP overlap
+
+DDP_LAYER_SHAPES = [(2048, 8192), (8192, 2048), (2048, 6144), (2048, 2048)]
+
+
+def ddp_overlap(args):
+    """The 1.2B-parameter DDP step on 8 emulated ranks: backward = per-rank
+    weight-gradient GEMMs dW = X^T dY (TF32, tokens x shapes below) written
+    straight into each rank's flat gradient buffer in reverse layer order;
+    communication = 185 x 25 MiB bucket all-reduces (ring, scale 1/8).  Four
+    variants, each one CUDA graph: compute only, comm only, compute then comm,
+    and overlapped (each bucket's all-reduce enqueued on a second stream as
+    soon as its gradients are written)."""
+    import torch
+
+    import __graft_entry__
+    import allreduce_reduction_emulated_gb300 as ar
+    from allreduce_reduction_emulated_gb300.buckets import BucketReducer
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    torch.backends.cuda.matmul.allow_tf32 = True
+    P, T, total, B = 8, args.tokens, DDP_PARAMS, DDP_BUCKET
+    grads = [torch.zeros(total, dtype=torch.float32, device=dev) for _ in range(P)]
+    outs = [torch.empty_like(g) for g in grads]
+    order = [(layer, i) for layer in reversed(range(24)) for i in range(4)]
+    views, off = [], 0
+    for layer, i in order:
+        m, n = DDP_LAYER_SHAPES[i]
+        views.append(([g[off:off + m * n].view(m, n) for g in grads], m, n, off + m * n))
+        off += m * n
+    assert off == total
+    gen = torch.Generator(device=dev).manual_seed(11)
+    acts = {d: [torch.randn(T, d, device=dev, generator=gen) * 0.01 for _ in range(P)] for d in (2048, 6144, 8192)}
+    comm = ar.ar_init(P)
+    compute = torch.cuda.Stream()
+    reducer = BucketReducer(comm, grads, B, scale=0.125, out=outs)
+    torch.cuda.synchronize()                    # inputs made on the default stream
+
+    def backward(overlap):
+        for vs, m, n, end in views:
+            for r in range(P):
+                torch.mm(acts[m][r].t(), acts[n][r], out=vs[r])
+            if overlap:
+                ev = torch.cuda.Event()
+                ev.record(compute)
+                reducer.ready(end, ev)
+
+    def variant(kind):
+        reducer.reset()
+        if kind in ("compute", "serial", "overlap"):
+            backward(kind == "overlap")
+        if kind in ("comm", "serial"):
+            ev = torch.cuda.Event()
+            ev.record(compute)
+            reducer.ready(total, ev)
+        if kind != "compute":
+            compute.wait_event(reducer.finish())
+
+    graphs = {}
+    for kind in ("compute", "comm", "serial", "overlap"):
+        with torch.cuda.stream(compute):
+            variant(kind)                       # warm-up outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(compute):
+            with torch.cuda.graph(g, stream=compute):
+                variant(kind)
+        graphs[kind] = g
+    times = {}
+    for kind, g in graphs.items():
+        for _ in range(max(args.warmup, 1)):
+            g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times[kind] = a.elapsed_time(b) / args.steps
+    if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+        raise SystemExit("device status error")
+    ar.ar_destroy(comm)
+    flops = P * 2.0 * total * T
+    model = max(times["compute"], times["comm"])
+    print(json.dumps({
+        "ddp_overlap": "P=8 x 1,207,959,552 fp32 gradients, 185 x 25 MiB buckets, ring, scale 1/8",
+        "tokens_per_rank": T, "steps": args.steps, "unit": "ms",
+        "compute_ms": times["compute"], "comm_ms": times["comm"], "serial_ms": times["serial"],
+        "overlap_ms": times["overlap"], "exposed_comm_ms": times["overlap"] - times["compute"],
+        "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,
+        "hidden_fraction_of_shorter": (times["serial"] - times["overlap"]) / min(times["compute"], times["comm"]),
+        "gemm_tflops": flops / (times["compute"] * 1e-3) / 1e12,
+        "comm_hbm_gbs": 2 * P * total * 4 / (times["comm"] * 1e-3) / 1e9,
+    }), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.ddp_overlap:
+        ddp_overlap(args)
+        return
     if args.ddp_buckets:
         ddp_buckets(args)
         return
