@@ -28,7 +28,8 @@ AR_SUCCESS, AR_ERR_INVALID_ARG, AR_ERR_CUDA, AR_ERR_UNSUPPORTED, AR_ERR_TIMEOUT,
 AR_FLOAT32, AR_BFLOAT16, AR_INT32 = 0, 1, 2
 AR_SUM, AR_MIN, AR_MAX = 0, 1, 2
 AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL, AR_ALGO_HIER = 0, 1, 2, 3, 4
-AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER, AR_OPT_HIER_GROUP = range(5)
+(AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER, AR_OPT_HIER_GROUP,
+ AR_OPT_MAX_BLOCKS) = range(6)
 AR_MAX_RANKS = 256
 AR_NOALLOC_MAX_RANKS, AR_NOALLOC_MAX_BYTES = 8, 65536
 

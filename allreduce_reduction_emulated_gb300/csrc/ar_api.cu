@@ -29,6 +29,7 @@ struct ar_comm {
   int16_t* tree_prog = nullptr;  // device: tree 0 program then tree 1 program
   int prog_len = 0;
   int hier_group = 8;            // AR_ALGO_HIER: ranks per group
+  int max_blocks = 0;            // AR_OPT_MAX_BLOCKS (0 = no cap)
 };
 
 namespace {
@@ -190,6 +191,7 @@ ar::Call base_call(ar_comm_t c, void* stream) {
   call.epoch = 0;
   call.shard = 0;
   call.group = c->hier_group;
+  call.max_blocks = c->max_blocks;
   call.algo = ar::kRing;
   call.scale = 1.0f;
   call.op = AR_SUM;
@@ -301,6 +303,10 @@ ar_status_t ar_set_option(ar_comm_t c, ar_option_t option, long long value) {
     case AR_OPT_LL_SKIP_PRODUCER:
       c->skip_produce = value != 0;
       return AR_SUCCESS;
+    case AR_OPT_MAX_BLOCKS:
+      if (value < 0 || value > 0x7fffffffll) return AR_ERR_INVALID_ARG;
+      c->max_blocks = (int)value;
+      return AR_SUCCESS;
     case AR_OPT_HIER_GROUP:
       if (value < 1 || value > c->P || c->P % value != 0) return AR_ERR_INVALID_ARG;
       c->hier_group = (int)value;
@@ -361,6 +367,7 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   call.op = op;
   call.algo = chosen == AR_ALGO_TREE ? ar::kTree : chosen == AR_ALGO_HIER ? ar::kHier : ar::kRing;
   call.group = c->hier_group;
+  call.max_blocks = c->max_blocks;
   call.scale = scale;
   call.stream = static_cast<cudaStream_t>(stream);
   call.sms = c->sms;

@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(kThreads) all_gather_elem_kernel(const __grid_
   }
 }
 
-unsigned grid_for(uint64_t items) {
+unsigned grid_for(uint64_t items, int max_blocks) {
   uint64_t g = (items + kThreads - 1) / kThreads;
+  if (max_blocks > 0 && g > (uint64_t)max_blocks) g = (uint64_t)max_blocks;
   return (unsigned)(g < 1 ? 1 : (g > 0x7fffffffull ? 0x7fffffffull : g));
 }
 
@@ -115,7 +116,7 @@ void fill(CollParams& p, const Call& c) {
 
 template <int DT>
 cudaError_t launch_rs_elem_dt(const Call& c, CollParams& p) {
-  const unsigned g = grid_for(p.total);
+  const unsigned g = grid_for(p.total, c.max_blocks);
   switch (c.op) {
     case kSum: reduce_scatter_elem_kernel<DT, kSum><<<g, kThreads, 0, c.stream>>>(p); break;
     case kMin: reduce_scatter_elem_kernel<DT, kMin><<<g, kThreads, 0, c.stream>>>(p); break;
@@ -132,7 +133,7 @@ cudaError_t launch_reduce_scatter_elem(const Call& c, LaunchInfo* info) {
   fill(p, c);
   p.total = (uint64_t)c.P * c.shard;
   info->kernel = "elementwise_reduce_scatter";
-  info->grid = (int)grid_for(p.total);
+  info->grid = (int)grid_for(p.total, c.max_blocks);
   info->block = kThreads;
   switch (c.dtype) {
     case kF32: return launch_rs_elem_dt<kF32>(c, p);
@@ -150,13 +151,13 @@ cudaError_t launch_all_gather(const Call& c, LaunchInfo* info) {
   if (c.algo == 1) {  // every pointer and the shard size are whole 16-byte units
     p.shard = c.shard * es / 16;  // vectors per shard
     p.total = (uint64_t)c.P * p.shard;
-    const unsigned g = grid_for(p.total);
+    const unsigned g = grid_for(p.total, c.max_blocks);
     all_gather_vec_kernel<<<g, kThreads, 0, c.stream>>>(p);
     info->kernel = "all_gather_vec";
     info->grid = (int)g;
   } else {
     p.total = (uint64_t)c.P * c.shard;
-    const unsigned g = grid_for(p.total);
+    const unsigned g = grid_for(p.total, c.max_blocks);
     if (es == 2) all_gather_elem_kernel<uint16_t><<<g, kThreads, 0, c.stream>>>(p);
     else all_gather_elem_kernel<uint32_t><<<g, kThreads, 0, c.stream>>>(p);
     info->kernel = "all_gather_elem";

@@ -154,72 +154,74 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
   }
   __syncthreads();
 
-  const uint64_t v = (uint64_t)blockIdx.x * kThreads + tid;
   const uint64_t n = p.nfull;
-  if (v > n || (v == n && p.tail == 0)) return;
-  const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
-  const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
-  const int16_t* ncomb = s_ncomb[t];
-  RankCursor<ALGO> cur;
-  cur.P = P;
-  cur.push = s_push[t];
-  if constexpr (ALGO == kRing) {
-    cur.a = first;
-  } else if constexpr (ALGO == kTree) {
-    cur.a = 0;
-  } else {
-    // hierarchical: intra-group chunk c1 (split = its length in vectors), then
-    // sub-chunk c2 of that chunk across the G groups
-    const uint64_t V = 16 / Lanes<DT>::kBytes;
-    const uint64_t c1 = v / p.split;
-    const uint64_t lo = c1 * p.split * V;
-    const uint64_t hi = lo + p.split * V < p.count ? lo + p.split * V : p.count;
-    const int G = P / p.Q;
-    const uint64_t L2v = ((hi - lo + G - 1) / G + V - 1) / V;
-    const uint64_t c2 = (v - c1 * p.split) / L2v;
-    cur.Q = p.Q;
-    cur.G = G;
-    cur.a0 = cur.a = (int)(c1 % (uint64_t)p.Q);
-    cur.b0 = cur.b = (int)c2;
-  }
-
-  Acc<DT> acc;
-  if (v < n) {
-    const uint32_t base = (uint32_t)__cvta_generic_to_shared(&slots[0][tid]);
-    constexpr uint32_t kSlotStride = kThreads * 16;
-#pragma unroll
-    for (int k = 0; k < kWindow; ++k) {
-      if (k < P) cp_async16(base + k * kSlotStride, s_send[cur.next()] + v);
-      cp_async_commit();
-    }
-    int j = 0;          // values consumed
-    int rd = 0;         // slot of value j
-    int wr = kWindow;   // slot for value j + kWindow
-    auto next = [&]() -> Acc<DT> {
-      cp_async_wait<kWindow - 1>();  // value j has landed
-      const uint4 raw = slots[rd][tid];
-      const int k = j + kWindow;
-      if (k < P) cp_async16(base + wr * kSlotStride, s_send[cur.next()] + v);
-      cp_async_commit();
-      ++j;
-      rd = rd + 1 == kSlots ? 0 : rd + 1;
-      wr = wr + 1 == kSlots ? 0 : wr + 1;
-      return widen<DT>(raw);
-    };
-    acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
-    cp_async_wait<0>();
-    const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
-    if constexpr (SCATTER) {
-      st_stream(s_recv[first] + (v - (uint64_t)first * p.split), o);
+  const uint64_t columns = n + (p.tail ? 1 : 0);
+  for (uint64_t v = (uint64_t)blockIdx.x * kThreads + tid; v < columns;
+       v += (uint64_t)gridDim.x * kThreads) {
+    const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
+    const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
+    const int16_t* ncomb = s_ncomb[t];
+    RankCursor<ALGO> cur;
+    cur.P = P;
+    cur.push = s_push[t];
+    if constexpr (ALGO == kRing) {
+      cur.a = first;
+    } else if constexpr (ALGO == kTree) {
+      cur.a = 0;
     } else {
-      for (int r = 0; r < P; ++r) st_stream(s_recv[r] + v, o);
+      // hierarchical: intra-group chunk c1 (split = its length in vectors), then
+      // sub-chunk c2 of that chunk across the G groups
+      const uint64_t V = 16 / Lanes<DT>::kBytes;
+      const uint64_t c1 = v / p.split;
+      const uint64_t lo = c1 * p.split * V;
+      const uint64_t hi = lo + p.split * V < p.count ? lo + p.split * V : p.count;
+      const int G = P / p.Q;
+      const uint64_t L2v = ((hi - lo + G - 1) / G + V - 1) / V;
+      const uint64_t c2 = (v - c1 * p.split) / L2v;
+      cur.Q = p.Q;
+      cur.G = G;
+      cur.a0 = cur.a = (int)(c1 % (uint64_t)p.Q);
+      cur.b0 = cur.b = (int)c2;
     }
-  } else {
-    // the trailing partial vector: element-wise loads, same order
-    auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[cur.next()] + n, p.tail)); };
-    acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
-    const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
-    for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
+
+    Acc<DT> acc;
+    if (v < n) {
+      const uint32_t base = (uint32_t)__cvta_generic_to_shared(&slots[0][tid]);
+      constexpr uint32_t kSlotStride = kThreads * 16;
+  #pragma unroll
+      for (int k = 0; k < kWindow; ++k) {
+        if (k < P) cp_async16(base + k * kSlotStride, s_send[cur.next()] + v);
+        cp_async_commit();
+      }
+      int j = 0;          // values consumed
+      int rd = 0;         // slot of value j
+      int wr = kWindow;   // slot for value j + kWindow
+      auto next = [&]() -> Acc<DT> {
+        cp_async_wait<kWindow - 1>();  // value j has landed
+        const uint4 raw = slots[rd][tid];
+        const int k = j + kWindow;
+        if (k < P) cp_async16(base + wr * kSlotStride, s_send[cur.next()] + v);
+        cp_async_commit();
+        ++j;
+        rd = rd + 1 == kSlots ? 0 : rd + 1;
+        wr = wr + 1 == kSlots ? 0 : wr + 1;
+        return widen<DT>(raw);
+      };
+      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
+      cp_async_wait<0>();
+      const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
+      if constexpr (SCATTER) {
+        st_stream(s_recv[first] + (v - (uint64_t)first * p.split), o);
+      } else {
+        for (int r = 0; r < P; ++r) st_stream(s_recv[r] + v, o);
+      }
+    } else {
+      // the trailing partial vector: element-wise loads, same order
+      auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[cur.next()] + n, p.tail)); };
+      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
+      const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
+      for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
+    }
   }
 }
 
@@ -247,7 +249,8 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   if (ALGO == kTree && c.prog_len > kMaxProg) return cudaErrorInvalidValue;
   const uint64_t columns = p.nfull + (p.tail ? 1 : 0);
-  const uint64_t grid = (columns + kThreads - 1) / kThreads;
+  uint64_t grid = (columns + kThreads - 1) / kThreads;
+  if (c.max_blocks > 0 && grid > (uint64_t)c.max_blocks) grid = (uint64_t)c.max_blocks;
   if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(p);
   info->kernel = ALGO == kRing ? "pipelined_ring" : ALGO == kHier ? "pipelined_hier" : "pipelined_tree";
@@ -295,7 +298,8 @@ cudaError_t launch_scatter_one(const Call& c, LaunchInfo* info) {
   p.split = c.shard / V;
   p.scale = c.scale;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
-  const uint64_t grid = (p.nfull + kThreads - 1) / kThreads;
+  uint64_t grid = (p.nfull + kThreads - 1) / kThreads;
+  if (c.max_blocks > 0 && grid > (uint64_t)c.max_blocks) grid = (uint64_t)c.max_blocks;
   if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
   kernel<<<(unsigned)grid, kThreads, 0, c.stream>>>(p);
   info->kernel = "pipelined_reduce_scatter";

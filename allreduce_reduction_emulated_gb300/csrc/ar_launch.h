@@ -34,6 +34,7 @@ struct Call {
   // count is then the length of the larger buffers (P * shard)
   size_t shard;
   int group;                    // hierarchical order: ranks per group
+  int max_blocks;               // > 0: at most this many CTAs (grid-stride loops)
   uint32_t epoch;
   uint32_t spin_limit;
   int skip_produce;

@@ -120,6 +120,9 @@ extern "C" ar_status_t ar_allreduce_ll_noalloc(int nranks, const void* const* se
     c.status = reinterpret_cast<int*>(s.base);
     c.spin_limit = kSpinLimit;
     c.skip_produce = 0;
+    c.max_blocks = 0;
+    c.group = 1;
+    c.shard = 0;
     cudaError_t e = cudaSuccess;
     {
       std::lock_guard<std::mutex> g(s.lock);

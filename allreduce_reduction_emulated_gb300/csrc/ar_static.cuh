@@ -149,7 +149,8 @@ cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
     return b > 0 ? b : 1;
   }();
   const uint64_t need = (p.nfull + kStaticThreads * U - 1) / (kStaticThreads * U);
-  const uint64_t cap = kStaticPersistent ? (uint64_t)c.sms * (uint64_t)blocks_per_sm : 0x7fffffffull;
+  uint64_t cap = kStaticPersistent ? (uint64_t)c.sms * (uint64_t)blocks_per_sm : 0x7fffffffull;
+  if (c.max_blocks > 0 && (uint64_t)c.max_blocks < cap) cap = (uint64_t)c.max_blocks;
   const int grid = (int)(need < 1 ? 1 : (need < cap ? need : cap));
   kernel<<<grid, kStaticThreads, 0, c.stream>>>(p);
   info->kernel = ALGO == kRing ? "static_ring" : "static_tree";

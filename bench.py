@@ -117,6 +117,10 @@ def parse_args():
                          "bucketed all-reduce: compute, comm, serial and overlapped step times")
     ap.add_argument("--tokens", type=int, default=512,
                     help="tokens per rank for --ddp-overlap's gradient GEMMs")
+    ap.add_argument("--comm-blocks", type=int, default=0,
+                    help="--ddp-overlap: cap the all-reduce kernels at this many thread blocks (0 = none)")
+    ap.add_argument("--comm-priority", action="store_true",
+                    help="--ddp-overlap: run the communication stream at the highest priority")
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep (P=8 fp32, 8 B .. 1 GiB per rank) with an alpha-beta fit")
     return ap.parse_args()
@@ -747,8 +751,11 @@ def ddp_overlap(args):
     gen = torch.Generator(device=dev).manual_seed(11)
     acts = {d: [torch.randn(T, d, device=dev, generator=gen) * 0.01 for _ in range(P)] for d in (2048, 6144, 8192)}
     comm = ar.ar_init(P)
+    if args.comm_blocks:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, args.comm_blocks)
     compute = torch.cuda.Stream()
-    reducer = BucketReducer(comm, grads, B, scale=0.125, out=outs)
+    high = torch.cuda.Stream.priority_range()[1] if args.comm_priority else 0
+    reducer = BucketReducer(comm, grads, B, scale=0.125, out=outs, stream=torch.cuda.Stream(priority=high))
     torch.cuda.synchronize()                    # inputs made on the default stream
 
     def backward(overlap):
@@ -802,6 +809,7 @@ def ddp_overlap(args):
     print(json.dumps({
         "ddp_overlap": "P=8 x 1,207,959,552 fp32 gradients, 185 x 25 MiB buckets, ring, scale 1/8",
         "tokens_per_rank": T, "steps": args.steps, "unit": "ms",
+        "comm_blocks": args.comm_blocks, "comm_priority": bool(args.comm_priority),
         "compute_ms": times["compute"], "comm_ms": times["comm"], "serial_ms": times["serial"],
         "overlap_ms": times["overlap"], "exposed_comm_ms": times["overlap"] - times["compute"],
         "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,

@@ -165,9 +165,14 @@ typedef enum {
     AR_OPT_DEBUG = 2,            /* nonzero: one line per call on stderr               */
     AR_OPT_LL_SKIP_PRODUCER = 3, /* test hook: LL kernels skip staging, so every flag
                                     wait runs out and reports AR_ERR_TIMEOUT           */
-    AR_OPT_HIER_GROUP = 4        /* AR_ALGO_HIER ranks per group: a divisor of P
+    AR_OPT_HIER_GROUP = 4,       /* AR_ALGO_HIER ranks per group: a divisor of P
                                     (default 8; a call whose P it does not divide
                                     returns AR_ERR_UNSUPPORTED)                       */
+    AR_OPT_MAX_BLOCKS = 5        /* > 0: ring / tree / hierarchical / reduce-scatter /
+                                    all-gather kernels launch at most this many
+                                    thread blocks (grid-stride), leaving the other
+                                    SMs to kernels on other streams; 0 = no cap
+                                    (default).  Results do not change.              */
 } ar_option_t;
 
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
