@@ -27,15 +27,16 @@ AR_SUCCESS, AR_ERR_INVALID_ARG, AR_ERR_CUDA, AR_ERR_UNSUPPORTED, AR_ERR_TIMEOUT,
 # ar_dtype_t, ar_op_t, ar_algo_t, ar_option_t
 AR_FLOAT32, AR_BFLOAT16, AR_INT32 = 0, 1, 2
 AR_SUM, AR_MIN, AR_MAX = 0, 1, 2
-AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL, AR_ALGO_HIER = 0, 1, 2, 3, 4
+AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL, AR_ALGO_HIER, AR_ALGO_LL128 = range(6)
 (AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER, AR_OPT_HIER_GROUP,
- AR_OPT_MAX_BLOCKS) = range(6)
+ AR_OPT_MAX_BLOCKS, AR_OPT_LL128_MAX_BYTES, AR_OPT_AUTO_TUNED) = range(8)
+AR_TUNE_BUCKETS = 22
 AR_MAX_RANKS = 256
 AR_NOALLOC_MAX_RANKS, AR_NOALLOC_MAX_BYTES = 8, 65536
 
 OPS = {"sum": AR_SUM, "min": AR_MIN, "max": AR_MAX}
 ALGOS = {"auto": AR_ALGO_AUTO, "ring": AR_ALGO_RING, "tree": AR_ALGO_TREE, "ll": AR_ALGO_LL,
-         "hier": AR_ALGO_HIER}
+         "hier": AR_ALGO_HIER, "ll128": AR_ALGO_LL128}
 
 
 class ArError(RuntimeError):
@@ -74,6 +75,8 @@ def library() -> ctypes.CDLL:
                 L.ar_select_algo.restype = i
                 L.ar_set_option.argtypes = [vp, i, ctypes.c_longlong]
                 L.ar_set_option.restype = i
+                L.ar_tune.argtypes = [vp, ctypes.POINTER(i), i]
+                L.ar_tune.restype = i
                 L.ar_reduce_scatter.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, i, i,
                                                  ctypes.c_float, vp]
                 L.ar_reduce_scatter.restype = i
@@ -170,6 +173,16 @@ def ar_select_algo(comm: int, count: int, dtype: int, algo: int = AR_ALGO_AUTO) 
     if st != AR_SUCCESS:
         raise ArError(st, "ar_select_algo")
     return out.value
+
+
+def ar_tune(comm: int) -> list:
+    """Times ring / tree / LL / LL128 per size on this device and makes AUTO use
+    the fastest; returns the chosen algorithm for 8 B, 16 B, ... 16 MiB per rank."""
+    table = (ctypes.c_int * AR_TUNE_BUCKETS)()
+    st = library().ar_tune(comm, table, AR_TUNE_BUCKETS)
+    if st != AR_SUCCESS:
+        raise ArError(st, "ar_tune")
+    return list(table)
 
 
 def ar_set_option(comm: int, option: int, value: int) -> None:

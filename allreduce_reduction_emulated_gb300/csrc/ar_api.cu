@@ -28,7 +28,17 @@ struct ar_comm {
   int* status = nullptr;         // device ar_status_t word
   int16_t* tree_prog = nullptr;  // device: tree 0 program then tree 1 program
   int prog_len = 0;
+  // LL128 staging: P slots of `ll128_stride` 8-byte words (128-byte lines)
+  unsigned long long* staging128 = nullptr;
+  size_t ll128_stride = 0;
+  size_t ll128_capacity_bytes = 0;
+  size_t ll128_max_bytes = 0;
   int hier_group = 8;            // AR_ALGO_HIER: ranks per group
+  // ar_tune: fastest algorithm per power-of-two size bucket, used by AUTO
+  // when auto_tuned is set
+  ar_algo_t tuned[AR_TUNE_BUCKETS] = {};
+  int tuned_valid = 0;
+  int auto_tuned = 0;
   int max_blocks = 0;            // AR_OPT_MAX_BLOCKS (0 = no cap)
 };
 
@@ -37,6 +47,8 @@ namespace {
 constexpr size_t kDefaultLLBytes = 65536;
 constexpr uint32_t kDefaultSpinLimit = 1u << 22;  // ~1 s of L2 polls at worst
 constexpr size_t kMaxLLBytes = 1u << 20;
+constexpr size_t kDefaultLL128Bytes = 1u << 20;
+constexpr size_t kMaxLL128Bytes = 16u << 20;
 
 long long env_ll(const char* name, long long dflt) {
   const char* s = std::getenv(name);
@@ -50,7 +62,7 @@ bool valid_dtype(int d) { return d == AR_FLOAT32 || d == AR_BFLOAT16 || d == AR_
 bool valid_op(int o) { return o == AR_SUM || o == AR_MIN || o == AR_MAX; }
 bool valid_algo(int a) {
   return a == AR_ALGO_AUTO || a == AR_ALGO_RING || a == AR_ALGO_TREE || a == AR_ALGO_LL ||
-         a == AR_ALGO_HIER;
+         a == AR_ALGO_HIER || a == AR_ALGO_LL128;
 }
 
 // Postorder program of tree t: push own rank, then each child's subtree
@@ -84,20 +96,39 @@ const char* algo_name(int a) {
          : a == AR_ALGO_TREE ? "tree"
          : a == AR_ALGO_LL   ? "ll"
          : a == AR_ALGO_HIER ? "hier"
+         : a == AR_ALGO_LL128 ? "ll128"
                              : "auto";
 }
 
 void release(ar_comm* c) {
   if (!c) return;
   if (c->staging) cudaFree(c->staging);
+  if (c->staging128) cudaFree(c->staging128);
   if (c->status) cudaFree(c->status);
   if (c->tree_prog) cudaFree(c->tree_prog);
   delete c;
 }
 
+// Bucket i of the tuning table covers per-rank sizes (2^(i+2), 2^(i+3)] bytes.
+int tune_bucket(size_t bytes) {
+  int i = 0;
+  size_t top = 8;
+  while (top < bytes && i < AR_TUNE_BUCKETS - 1) {
+    top <<= 1;
+    ++i;
+  }
+  return i;
+}
+
 ar_algo_t resolve(const ar_comm* c, size_t count, ar_dtype_t dtype, ar_algo_t algo) {
   if (algo != AR_ALGO_AUTO) return algo;
   const size_t bytes = count * ar::elem_bytes(dtype);
+  if (c->auto_tuned && c->tuned_valid) {
+    ar_algo_t a = c->tuned[tune_bucket(bytes)];
+    if (a == AR_ALGO_LL && bytes > c->ll_max_bytes) a = AR_ALGO_RING;
+    if (a == AR_ALGO_LL128 && bytes > c->ll128_max_bytes) a = AR_ALGO_RING;
+    return a;
+  }
   return bytes <= c->ll_max_bytes ? AR_ALGO_LL : AR_ALGO_RING;
 }
 
@@ -238,6 +269,13 @@ ar_status_t ar_init(int nranks, ar_comm_t* out) {
 
   c->stage_stride = (c->ll_capacity_bytes + 3) / 4 + 4;
   const size_t stage_bytes = (size_t)nranks * c->stage_stride * sizeof(unsigned long long);
+  long long ll128 = env_ll("AR_LL128_MAX_BYTES", (long long)kDefaultLL128Bytes);
+  if (ll128 < 16) ll128 = 16;
+  if (ll128 > (long long)kMaxLL128Bytes) ll128 = (long long)kMaxLL128Bytes;
+  c->ll128_capacity_bytes = (size_t)ll128;
+  c->ll128_max_bytes = (size_t)ll128;
+  c->ll128_stride = ar::ll128_stage_words(c->ll128_capacity_bytes);
+  const size_t stage128_bytes = (size_t)nranks * c->ll128_stride * sizeof(unsigned long long);
   std::vector<int16_t> prog;
   for (int t = 0; t < 2; ++t) emit_tree(ar::tree_root(nranks), nranks, t, prog);
   c->prog_len = (int)prog.size() / 2;
@@ -246,6 +284,8 @@ ar_status_t ar_init(int nranks, ar_comm_t* out) {
     return AR_ERR_INVALID_ARG;
   }
   cudaError_t e = cudaMalloc(&c->staging, stage_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&c->staging128, stage128_bytes);
+  if (e == cudaSuccess) e = cudaMemset(c->staging128, 0, stage128_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&c->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMalloc(&c->tree_prog, prog.size() * sizeof(int16_t));
   if (e == cudaSuccess) e = cudaMemset(c->staging, 0, stage_bytes);
@@ -303,6 +343,14 @@ ar_status_t ar_set_option(ar_comm_t c, ar_option_t option, long long value) {
     case AR_OPT_LL_SKIP_PRODUCER:
       c->skip_produce = value != 0;
       return AR_SUCCESS;
+    case AR_OPT_LL128_MAX_BYTES:
+      if (value < 16 || (size_t)value > c->ll128_capacity_bytes) return AR_ERR_INVALID_ARG;
+      c->ll128_max_bytes = (size_t)value;
+      return AR_SUCCESS;
+    case AR_OPT_AUTO_TUNED:
+      if (value != 0 && !c->tuned_valid) return AR_ERR_INVALID_ARG;  // run ar_tune first
+      c->auto_tuned = value != 0;
+      return AR_SUCCESS;
     case AR_OPT_MAX_BLOCKS:
       if (value < 0 || value > 0x7fffffffll) return AR_ERR_INVALID_ARG;
       c->max_blocks = (int)value;
@@ -341,9 +389,10 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
 
   ar_algo_t chosen = resolve(c, count, dtype, algo);
   if (chosen == AR_ALGO_LL && count * esize > c->ll_max_bytes) return AR_ERR_UNSUPPORTED;
+  if (chosen == AR_ALGO_LL128 && count * esize > c->ll128_max_bytes) return AR_ERR_UNSUPPORTED;
   if (chosen == AR_ALGO_HIER && P % c->hier_group != 0) return AR_ERR_UNSUPPORTED;
-  if (chosen == AR_ALGO_LL) {
-    // The LL epoch is a launch parameter: a captured launch would replay one
+  if (chosen == AR_ALGO_LL || chosen == AR_ALGO_LL128) {
+    // The LL / LL128 epoch is a launch parameter: a captured launch would replay one
     // epoch forever and could accept a previous replay's staged words.  Under
     // capture AUTO takes the ring (the same result bit for bit: LL folds in
     // the ring order) and a forced LL is refused.
@@ -383,11 +432,14 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
 
   ar::LaunchInfo info;
   cudaError_t e;
-  if (chosen == AR_ALGO_LL) {
+  if (chosen == AR_ALGO_LL || chosen == AR_ALGO_LL128) {
     if (c->epoch == 0xffffffffu) {
-      // every flag value has been used once: clear the staging and restart
+      // every flag value has been used once: clear both staging areas and restart
       e = cudaMemsetAsync(c->staging, 0, (size_t)P * c->stage_stride * sizeof(unsigned long long),
                           call.stream);
+      if (e == cudaSuccess)
+        e = cudaMemsetAsync(c->staging128, 0, (size_t)P * c->ll128_stride * sizeof(unsigned long long),
+                            call.stream);
       if (e != cudaSuccess) {
         cudaGetLastError();
         return AR_ERR_CUDA;
@@ -395,7 +447,13 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
       c->epoch = 0;
     }
     call.epoch = ++c->epoch;
-    e = ar::launch_ll(call, &info);
+    if (chosen == AR_ALGO_LL) {
+      e = ar::launch_ll(call, &info);
+    } else {
+      call.staging = c->staging128;
+      call.stage_stride = c->ll128_stride;
+      e = ar::launch_ll128(call, &info);
+    }
   } else if (chosen == AR_ALGO_HIER) {
     e = ar::launch_generic(call, &info);
   } else if (P <= ar::kMaxStaticRanks) {
@@ -471,6 +529,85 @@ ar_status_t ar_all_gather(ar_comm_t c, const void* const* sendbufs, void* const*
   if (e != cudaSuccess) {
     cudaGetLastError();
     return AR_ERR_CUDA;
+  }
+  return AR_SUCCESS;
+}
+
+ar_status_t ar_tune(ar_comm_t c, ar_algo_t* table, int table_len) {
+  if (!c || table_len < 0 || (table_len > 0 && !table)) return AR_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  if (dev != c->device) return AR_ERR_INVALID_ARG;
+  const int P = c->P;
+  const size_t top = (size_t)8 << (AR_TUNE_BUCKETS - 1);  // largest tuned size per rank
+  std::vector<void*> bufs(2 * (size_t)P, nullptr);
+  cudaStream_t s = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  ar_status_t st = AR_SUCCESS;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  for (size_t i = 0; e == cudaSuccess && i < bufs.size(); ++i) {
+    e = cudaMalloc(&bufs[i], top);
+    if (e == cudaSuccess) e = cudaMemset(bufs[i], 0, top);
+  }
+  const int saved_auto = c->auto_tuned;
+  c->auto_tuned = 0;
+  ar_algo_t result[AR_TUNE_BUCKETS];
+  const ar_algo_t candidates[] = {AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL, AR_ALGO_LL128};
+  constexpr int kReps = 20;
+  for (int b = 0; e == cudaSuccess && st == AR_SUCCESS && b < AR_TUNE_BUCKETS; ++b) {
+    const size_t count = ((size_t)8 << b) / 4;  // fp32 elements per rank
+    float best = 0.f;
+    result[b] = AR_ALGO_RING;
+    for (ar_algo_t a : candidates) {
+      if (a == AR_ALGO_LL && count * 4 > c->ll_max_bytes) continue;
+      if (a == AR_ALGO_LL128 && count * 4 > c->ll128_max_bytes) continue;
+      for (int k = 0; k < 2 && st == AR_SUCCESS; ++k)
+        st = ar_allreduce(c, bufs.data(), bufs.data() + P, count, AR_FLOAT32, AR_SUM, a, 1.0f, s);
+      if (st == AR_SUCCESS) e = cudaEventRecord(e0, s);
+      for (int k = 0; k < kReps && st == AR_SUCCESS && e == cudaSuccess; ++k)
+        st = ar_allreduce(c, bufs.data(), bufs.data() + P, count, AR_FLOAT32, AR_SUM, a, 1.0f, s);
+      if (st != AR_SUCCESS || e != cudaSuccess) break;
+      e = cudaEventRecord(e1, s);
+      if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+      float ms = 0.f;
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+      if (e != cudaSuccess) break;
+      if (best == 0.f || ms < best) {
+        best = ms;
+        result[b] = a;
+      }
+    }
+  }
+  if (e == cudaSuccess && st == AR_SUCCESS) {
+    ar_status_t dst = ar_get_status(c);  // a timed-out LL wait would void the timings
+    if (dst != AR_SUCCESS) st = dst;
+  }
+  for (void* p : bufs)
+    if (p) cudaFree(p);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (s) cudaStreamDestroy(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    st = e == cudaErrorMemoryAllocation ? AR_ERR_OOM : AR_ERR_CUDA;
+  }
+  if (st != AR_SUCCESS) {
+    c->auto_tuned = saved_auto;
+    return st;
+  }
+  for (int b = 0; b < AR_TUNE_BUCKETS; ++b) c->tuned[b] = result[b];
+  for (int b = 0; b < table_len && b < AR_TUNE_BUCKETS; ++b) table[b] = result[b];
+  c->tuned_valid = 1;
+  c->auto_tuned = 1;
+  if (c->debug) {
+    std::fprintf(stderr, "[ar] tune P=%d:", P);
+    for (int b = 0; b < AR_TUNE_BUCKETS; ++b) std::fprintf(stderr, " %zuB=%s", (size_t)8 << b, algo_name(result[b]));
+    std::fprintf(stderr, "\n");
   }
   return AR_SUCCESS;
 }

@@ -57,6 +57,9 @@ cudaError_t launch_static_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
 cudaError_t launch_generic(const Call& c, LaunchInfo* info);
 cudaError_t launch_ll(const Call& c, LaunchInfo* info);
+// LL128: 128-byte lines of 120 payload bytes + a flag word (staging, stage_stride)
+cudaError_t launch_ll128(const Call& c, LaunchInfo* info);
+size_t ll128_stage_words(size_t bytes_per_rank);
 // reduce-scatter with shards of whole 16-byte vectors (pipelined ring kernel)
 cudaError_t launch_reduce_scatter_vec(const Call& c, LaunchInfo* info);
 // reduce-scatter of any shard length, element by element (same order)

@@ -1,0 +1,278 @@
+// ar_ll128.cu -- the LL128 medium-message all-reduce.
+//
+// "Demystifying NVSHMEM" (the collectives paragraph) names LL128 next to LL:
+// data and arrival flag travel together, here in 128-byte lines of 16 words
+// of 8 bytes -- 15 payload words (120 bytes) and one flag word (this call's
+// epoch) -- so 94% of the staged bytes are payload against LL's 50%.
+// Whole-line atomicity of a 128-byte store is not a guarantee of the PTX
+// memory model, so the line is published explicitly: the lanes of a warp
+// write the payload words, fence, synchronise, and one lane stores the flag
+// word with release semantics; a reader acquires the flag and only then reads
+// the payload.  Emulated like LL inside one cooperative kernel: block group g
+// stages rank g's lines, then reduces ring chunk g in ring order (so LL128 ==
+// RING bit for bit) and writes the result into every rank's receive buffer.
+// Every flag wait is bounded; on its limit a thread records AR_ERR_TIMEOUT.
+#include "../../include/ar.h"
+#include "ar_device.cuh"
+#include "ar_launch.h"
+
+namespace ar {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLineWords = 16;     // 8-byte words per 128-byte line
+constexpr int kPayloadWords = 15;  // the 16th word is the flag
+constexpr int kBatch = 8;          // ranks polled together
+
+template <int MAXP>
+struct LL128Params {
+  const void* send[MAXP];
+  void* recv[MAXP];
+  unsigned long long* staging;  // P slots of `stride` 8-byte words (whole lines)
+  uint64_t stride;
+  int* status;
+  uint64_t nbytes;       // bytes per rank
+  uint64_t nwords;       // 8-byte payload words per rank
+  uint64_t nlines;       // lines per rank
+  uint64_t chunk_words;  // payload words per ring chunk (16-byte chunks: even)
+  uint32_t epoch;
+  uint32_t spin_limit;
+  int P;
+  int bpr;
+  int skip_produce;
+  int do_scale;
+  float scale;
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// 8-byte payload word w of a rank buffer (zero beyond nbytes).
+__device__ __forceinline__ unsigned long long load_word8(const void* buf, uint64_t w, uint64_t nbytes) {
+  if (8 * w + 8 <= nbytes) return static_cast<const unsigned long long*>(buf)[w];
+  unsigned long long v = 0;
+  const uint16_t* h = static_cast<const uint16_t*>(buf);
+  for (uint64_t b = 8 * w; b < nbytes; b += 2) v |= (unsigned long long)h[b / 2] << (8 * (b - 8 * w));
+  return v;
+}
+
+__device__ __forceinline__ void store_word8(void* buf, uint64_t w, uint64_t nbytes, unsigned long long v) {
+  if (8 * w + 8 <= nbytes) {
+    static_cast<unsigned long long*>(buf)[w] = v;
+    return;
+  }
+  uint16_t* h = static_cast<uint16_t*>(buf);
+  for (uint64_t b = 8 * w; b < nbytes; b += 2) h[b / 2] = (uint16_t)(v >> (8 * (b - 8 * w)));
+}
+
+// An 8-byte payload word holds 2 fp32 / int32 or 4 bf16 values.
+template <int DT> struct Word8 {
+  static constexpr int N = DT == kBF16 ? 4 : 2;
+  typename Lanes<DT>::T v[N];
+};
+
+template <int DT>
+__device__ __forceinline__ Word8<DT> widen8(unsigned long long x) {
+  Word8<DT> a;
+  const uint32_t lo = (uint32_t)x, hi = (uint32_t)(x >> 32);
+  if constexpr (DT == kF32) {
+    a.v[0] = __uint_as_float(lo);
+    a.v[1] = __uint_as_float(hi);
+  } else if constexpr (DT == kBF16) {
+    a.v[0] = bf16_lo(lo); a.v[1] = bf16_hi(lo); a.v[2] = bf16_lo(hi); a.v[3] = bf16_hi(hi);
+  } else {
+    a.v[0] = (int32_t)lo;
+    a.v[1] = (int32_t)hi;
+  }
+  return a;
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ void fold8(Word8<DT>& acc, const Word8<DT>& x) {
+#pragma unroll
+  for (int i = 0; i < Word8<DT>::N; ++i) acc.v[i] = combine<DT, OP>(acc.v[i], x.v[i]);
+}
+
+template <int DT>
+__device__ __forceinline__ unsigned long long narrow8(Word8<DT> a, float scale, bool do_scale) {
+  if constexpr (DT == kI32) {
+    return (unsigned long long)(uint32_t)a.v[0] | ((unsigned long long)(uint32_t)a.v[1] << 32);
+  } else {
+    if (do_scale) {
+#pragma unroll
+      for (int i = 0; i < Word8<DT>::N; ++i) a.v[i] = __fmul_rn(a.v[i], scale);
+    }
+    if constexpr (DT == kF32)
+      return (unsigned long long)__float_as_uint(a.v[0]) | ((unsigned long long)__float_as_uint(a.v[1]) << 32);
+    else
+      return (unsigned long long)pack_bf16x2(a.v[0], a.v[1]) |
+             ((unsigned long long)pack_bf16x2(a.v[2], a.v[3]) << 32);
+  }
+}
+
+template <int MAXP, int DT, int OP>
+__global__ void __launch_bounds__(kThreads) ll128_allreduce_kernel(const __grid_constant__ LL128Params<MAXP> p) {
+  const int P = p.P;
+  const int g = blockIdx.x / p.bpr;
+  const int lane = threadIdx.x & 31;
+  const unsigned long long flag = (unsigned long long)p.epoch;
+
+  // produce: a warp writes 4 lines at a time, 8 lanes per line (16 bytes
+  // each); lane 7 of each line then publishes the line with its flag word
+  if (!p.skip_produce) {
+    unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
+    const uint64_t warps = (uint64_t)p.bpr * (kThreads / 32);
+    const uint64_t warp = (uint64_t)(blockIdx.x % p.bpr) * (kThreads / 32) + threadIdx.x / 32;
+    const int part = lane & 7;  // 16-byte part of the line
+    for (uint64_t base = warp * 4; base < p.nlines; base += warps * 4) {
+      const uint64_t line = base + (uint64_t)(lane >> 3);
+      const bool live = line < p.nlines;
+      const uint64_t w0 = line * kPayloadWords + 2 * part;  // payload words of this part
+      if (live) {
+        slot[line * kLineWords + 2 * part] = w0 < p.nwords ? load_word8(p.send[g], w0, p.nbytes) : 0ull;
+        if (part < 7)
+          slot[line * kLineWords + 2 * part + 1] =
+              w0 + 1 < p.nwords ? load_word8(p.send[g], w0 + 1, p.nbytes) : 0ull;
+      }
+      __threadfence();  // each lane's payload words before the warp barrier ...
+      __syncwarp();
+      // ... and the flag after it, with release: a reader that acquires the
+      // flag sees the whole line
+      if (live && part == 7) st_release_u64(slot + line * kLineWords + kPayloadWords, flag);
+    }
+  }
+
+  // reduce ring chunk g: one 8-byte payload word per thread per step
+  const uint64_t lt = (uint64_t)(blockIdx.x % p.bpr) * kThreads + threadIdx.x;
+  const uint64_t nt = (uint64_t)p.bpr * kThreads;
+  const uint64_t w0 = (uint64_t)g * p.chunk_words;
+  uint64_t w1 = w0 + p.chunk_words;
+  if (w1 > p.nwords) w1 = p.nwords;
+  for (uint64_t w = w0 + lt; w < w1; w += nt) {
+    const uint64_t line = w / kPayloadWords;
+    const uint64_t off = line * kLineWords + (w - line * kPayloadWords);
+    Word8<DT> acc;
+    for (int k0 = 0; k0 < P; k0 += kBatch) {
+      unsigned long long f[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int k = k0 + j;
+        if (k < P) {
+          int r = g + k;
+          if (r >= P) r -= P;
+          f[j] = ld_acquire_u64(p.staging + (uint64_t)r * p.stride + line * kLineWords + kPayloadWords);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int k = k0 + j;
+        if (k >= P) break;
+        int r = g + k;
+        if (r >= P) r -= P;
+        const unsigned long long* fl = p.staging + (uint64_t)r * p.stride + line * kLineWords + kPayloadWords;
+        uint32_t spins = 0;
+        while (f[j] != flag) {
+          if (++spins > p.spin_limit) {
+            atomicExch(p.status, (int)AR_ERR_TIMEOUT);
+            return;
+          }
+          f[j] = ld_acquire_u64(fl);
+        }
+        const Word8<DT> x = widen8<DT>(ld_relaxed_u64(p.staging + (uint64_t)r * p.stride + off));
+        if (k == 0) acc = x;
+        else fold8<DT, OP>(acc, x);
+      }
+    }
+    const unsigned long long out = narrow8<DT>(acc, p.scale, p.do_scale != 0);
+    for (int r = 0; r < P; ++r) store_word8(p.recv[r], w, p.nbytes, out);
+  }
+}
+
+template <int MAXP, int DT, int OP>
+cudaError_t launch_one(const Call& c, LaunchInfo* info) {
+  auto kernel = ll128_allreduce_kernel<MAXP, DT, OP>;
+  LL128Params<MAXP> p;
+  for (int r = 0; r < c.P; ++r) {
+    p.send[r] = c.send[r];
+    p.recv[r] = c.recv[r];
+  }
+  p.staging = c.staging;
+  p.stride = c.stage_stride;
+  p.status = c.status;
+  p.nbytes = c.count * elem_bytes(DT);
+  p.nwords = (p.nbytes + 7) / 8;
+  p.nlines = (p.nwords + kPayloadWords - 1) / kPayloadWords;
+  p.chunk_words = ring_chunk_vectors(c.count, c.P, DT) * 2;  // 16-byte vectors = 2 words
+  p.epoch = c.epoch;
+  p.spin_limit = c.spin_limit;
+  p.P = c.P;
+  p.skip_produce = c.skip_produce;
+  p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
+  p.scale = c.scale;
+  if (p.nlines * kLineWords > p.stride) return cudaErrorInvalidValue;
+  static const int blocks_per_sm = [&] {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess) b = 0;
+    return b;
+  }();
+  const int resident = blocks_per_sm * c.sms;
+  if (c.P > resident) return cudaErrorCooperativeLaunchTooLarge;
+  uint64_t bpr = (p.nlines * 8 + kThreads - 1) / kThreads;  // 8 lanes per line when producing
+  const uint64_t bpr_cap = (uint64_t)(resident / c.P);
+  if (bpr > bpr_cap) bpr = bpr_cap;
+  if (bpr < 1) bpr = 1;
+  p.bpr = (int)bpr;
+  const int grid = c.P * p.bpr;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchCooperativeKernel((const void*)kernel, dim3(grid), dim3(kThreads), args, 0,
+                                              c.stream);
+  info->kernel = "ll128";
+  info->grid = grid;
+  info->block = kThreads;
+  info->smem = 0;
+  return e;
+}
+
+template <int MAXP, int DT>
+cudaError_t launch_op(const Call& c, LaunchInfo* info) {
+  switch (c.op) {
+    case kSum: return launch_one<MAXP, DT, kSum>(c, info);
+    case kMin: return launch_one<MAXP, DT, kMin>(c, info);
+    case kMax: return launch_one<MAXP, DT, kMax>(c, info);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int MAXP>
+cudaError_t launch_dt(const Call& c, LaunchInfo* info) {
+  switch (c.dtype) {
+    case kF32: return launch_op<MAXP, kF32>(c, info);
+    case kBF16: return launch_op<MAXP, kBF16>(c, info);
+    case kI32: return launch_op<MAXP, kI32>(c, info);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+// Staged 8-byte words per rank for an LL128 limit of `bytes` per rank.
+size_t ll128_stage_words(size_t bytes) {
+  const size_t words = (bytes + 7) / 8;
+  const size_t lines = (words + kPayloadWords - 1) / kPayloadWords;
+  return lines * kLineWords;
+}
+
+cudaError_t launch_ll128(const Call& c, LaunchInfo* info) {
+  if (c.P <= 8) return launch_dt<8>(c, info);
+  return launch_dt<AR_MAX_RANKS>(c, info);
+}
+
+}  // namespace ar

@@ -554,7 +554,7 @@ def sweep(args):
     comm = ar.ar_init(P)
     stream = torch.cuda.current_stream()
     names = {ar.AR_ALGO_AUTO: "auto", ar.AR_ALGO_RING: "ring", ar.AR_ALGO_TREE: "tree",
-             ar.AR_ALGO_LL: "ll"}
+             ar.AR_ALGO_LL: "ll", ar.AR_ALGO_LL128: "ll128"}
     rows = []
     count = 2
     while count <= top:
@@ -565,6 +565,8 @@ def sweep(args):
         algos = [ar.AR_ALGO_AUTO, ar.AR_ALGO_RING, ar.AR_ALGO_TREE]
         if nbytes <= 65536:
             algos.append(ar.AR_ALGO_LL)
+        if nbytes <= 1 << 20:
+            algos.append(ar.AR_ALGO_LL128)
         for algo in algos:
             def call():
                 ar.ar_allreduce(comm, sends, recvs, count, ar.AR_FLOAT32, ar.AR_SUM, algo, 1.0, stream)
@@ -601,16 +603,18 @@ def sweep(args):
                          "busbw": nbytes / t / 1e9 * 2 * (P - 1) / P,
                          "hbm_gbs": 2 * P * nbytes / t / 1e9, "l2_flushed": small})
         count *= 2
+    table = ar.ar_tune(comm)
     ar.ar_destroy(comm)
     fits = {}
-    for name in ("ring", "tree", "ll", "auto"):
+    for name in ("ring", "tree", "ll", "ll128", "auto"):
         pts = [(r["bytes_per_rank"], r["us"] * 1e-6) for r in rows if r["algo"] == name]
         if len(pts) >= 2:
             alpha, beta = fit_alpha_beta(pts)
             fits[name] = {"alpha_us": alpha * 1e6, "inv_beta_gbs": (1 / beta / 1e9) if beta > 0 else None,
                           "points": len(pts)}
     print(json.dumps({"sweep": "P=8 fp32 uniform[-1,1] sum, bytes per rank 8 B .. 1 GiB (x2)",
-                      "unit": "us / GB/s", "rows": rows, "fit": fits}), flush=True)
+                      "unit": "us / GB/s", "rows": rows, "fit": fits,
+                      "ar_tune_table": {str(8 << b): names[a] for b, a in enumerate(table)}}), flush=True)
 
 
 # ------------------------------------------------------------ DDP buckets

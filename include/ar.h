@@ -33,6 +33,13 @@
  *     atomic write): each rank's 4-byte payload words are staged as 8-byte
  *     {payload, flag = per-call epoch} words, reducers poll the flags (bounded
  *     spin) and fold in the RING order, so LL == RING bit for bit.
+ *   AR_ALGO_LL128 -- LL's medium-message sibling (same paragraph of
+ *     "Demystifying NVSHMEM"): each rank's bytes are staged in 128-byte lines
+ *     of 120 payload bytes and one flag word (the epoch).  A 128-byte store is
+ *     not guaranteed to be seen whole by the PTX memory model, so a line is
+ *     published with a release store of its flag after the payload, and read
+ *     after an acquire of the flag.  Ring order: LL128 == RING bit for bit.
+ *     Up to the LL128 limit (1 MiB per rank by default, AR_LL128_MAX_BYTES).
  *   AR_ALGO_HIER -- the hierarchical all-reduce (lecture_068 page, section 06:
  *     reduce-scatter inside each node, ring all-reduce between nodes,
  *     all-gather inside each node) for P = G groups of Q consecutive ranks
@@ -45,7 +52,8 @@
  *     the plain ring.  Never chosen by AUTO.
  *   AR_ALGO_AUTO -- LL when count * sizeof(element) <= the LL limit (64 KiB by
  *     default), RING above it (NCCL picks tree for small and ring for large
- *     messages by itself: "NCCL and NVSHMEM ...", the ring / tree paragraph).
+ *     messages by itself: "NCCL and NVSHMEM ...", the ring / tree paragraph);
+ *     after ar_tune, the measured fastest algorithm for the size instead.
  * Accumulation: fp32 for fp32 and bf16 data (bf16 rounded once, to nearest
  * even, at the end), two's-complement wrap-around for int32.  Min / max keep
  * the earlier operand of a tie in fold order.
@@ -86,18 +94,24 @@ typedef enum {
     AR_ALGO_RING = 1,
     AR_ALGO_TREE = 2,
     AR_ALGO_LL = 3,
-    AR_ALGO_HIER = 4
+    AR_ALGO_HIER = 4,
+    AR_ALGO_LL128 = 5
 } ar_algo_t;
 
 /* Largest number of emulated ranks one communicator takes. */
 #define AR_MAX_RANKS 256
 
+/* Size buckets measured by ar_tune: per-rank sizes 8 B, 16 B, ..., 16 MiB. */
+#define AR_TUNE_BUCKETS 22
+
 /*
  * Creates a communicator for `nranks` emulated ranks (1 .. AR_MAX_RANKS) on
  * the calling thread's current CUDA device and stores it in *out.  Allocates
  * the LL staging area (nranks * LL limit * 2 bytes: 8-byte words carrying
- * 4-byte payloads), a device status word and the tree schedules; reads the
- * environment defaults AR_DEBUG, AR_LL_MAX_BYTES and AR_LL_SPIN_LIMIT.
+ * 4-byte payloads), the LL128 staging area (nranks * LL128 limit * 128/120
+ * bytes), a device status word and the tree schedules; reads the
+ * environment defaults AR_DEBUG, AR_LL_MAX_BYTES, AR_LL128_MAX_BYTES and
+ * AR_LL_SPIN_LIMIT.
  * Synchronous.  Errors: AR_ERR_INVALID_ARG (out == NULL or nranks out of
  * range), AR_ERR_CUDA (no usable device), AR_ERR_OOM.  On error *out is NULL.
  */
@@ -124,10 +138,11 @@ ar_status_t ar_init(int nranks, ar_comm_t* out);
  * AR_ERR_UNSUPPORTED) before anything is enqueued; launch failures return
  * AR_ERR_CUDA; device-side errors (LL spin limit) are reported later by
  * ar_get_status.
- * CUDA graphs: RING and TREE calls may be captured and replayed (the buffers
- * are then fixed).  LL calls are not capturable -- each call needs a fresh
- * epoch -- so while `stream` is capturing, AUTO resolves to RING (identical
- * result) and a forced AR_ALGO_LL returns AR_ERR_UNSUPPORTED.
+ * CUDA graphs: RING, TREE and HIER calls may be captured and replayed (the
+ * buffers are then fixed).  LL and LL128 calls are not capturable -- each
+ * call needs a fresh epoch -- so while `stream` is capturing, AUTO resolves
+ * to RING (identical result) and a forced AR_ALGO_LL / AR_ALGO_LL128 returns
+ * AR_ERR_UNSUPPORTED.
  */
 ar_status_t ar_allreduce(ar_comm_t comm, const void* const* sendbufs, void* const* recvbufs,
                          size_t count, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,
@@ -168,6 +183,11 @@ typedef enum {
     AR_OPT_HIER_GROUP = 4,       /* AR_ALGO_HIER ranks per group: a divisor of P
                                     (default 8; a call whose P it does not divide
                                     returns AR_ERR_UNSUPPORTED)                       */
+    AR_OPT_LL128_MAX_BYTES = 6,  /* LL128 limit in bytes per rank, 16 .. the size given
+                                    at ar_init (default 1 MiB or AR_LL128_MAX_BYTES)   */
+    AR_OPT_AUTO_TUNED = 7,       /* nonzero: AUTO follows the table measured by
+                                    ar_tune; 0: the fixed LL-up-to-the-limit rule
+                                    (default; ar_tune sets it to 1)                  */
     AR_OPT_MAX_BLOCKS = 5        /* > 0: ring / tree / hierarchical / reduce-scatter /
                                     all-gather kernels launch at most this many
                                     thread blocks (grid-stride), leaving the other
@@ -176,6 +196,24 @@ typedef enum {
 } ar_option_t;
 
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
+
+/*
+ * Measures which algorithm is fastest on this device for this communicator's
+ * rank count and makes AUTO use the result.  NCCL picks among ring, tree and
+ * its protocols by message size and hardware, and the crossover has to be
+ * measured per platform ("NCCL and NVSHMEM -- two GPU communication models,
+ * side by side": the ring / tree paragraph and exercise 6, force each
+ * algorithm and find the crossover; "Demystifying NVSHMEM": selection is a
+ * rule table, not an analytic model).  For every per-rank size 8 B * 2^i,
+ * i < AR_TUNE_BUCKETS, it times RING, TREE, LL and LL128 (fp32 sum, 20 calls
+ * back to back, within the LL / LL128 limits) and keeps the fastest; AUTO
+ * then rounds a call's size up to a bucket and uses its entry.
+ *   table  optional (table_len entries): the chosen algorithm per bucket.
+ * Synchronous; allocates and frees 2 * nranks * 16 MiB of scratch buffers and
+ * a stream.  Errors: AR_ERR_INVALID_ARG, AR_ERR_OOM, AR_ERR_CUDA, or the
+ * status of a failed measurement call (the previous AUTO rule is kept).
+ */
+ar_status_t ar_tune(ar_comm_t comm, ar_algo_t* table, int table_len);
 
 /*
  * Reduce-scatter ("NCCL, NIXL, and Distributed GPU Communication", section

@@ -1,0 +1,122 @@
+"""LL128 (128-byte lines: 120 payload bytes + a release-published flag word)
+against the oracle's ring order, bit for bit ("Demystifying NVSHMEM", the
+collectives paragraph: LL / LL128 pack data and arrival flag together)."""
+import numpy as np
+import pytest
+import torch
+
+import allreduce_reduction_emulated_gb300 as ar
+import oracle
+import pins
+from gpu_util import Guarded, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def line_counts(dtype):
+    """Counts around whole 120-byte lines and up to the 1 MiB limit."""
+    per_line = 60 if dtype == ar.AR_BFLOAT16 else 30
+    top = (1 << 20) // (2 if dtype == ar.AR_BFLOAT16 else 4)
+    return sorted({1, per_line - 1, per_line, per_line + 1, 2 * per_line + 1, 1000, 12345, top - 1, top})
+
+
+@pytest.mark.parametrize("P", [1, 2, 8, 13])
+@pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
+def test_ll128_line_boundaries_and_limit(P, dtype, dev):
+    rng = np.random.default_rng(70 + P + 10 * dtype)
+    comm = ar.ar_init(P)
+    try:
+        for count in line_counts(dtype):
+            sends = pins.random_inputs(rng, P, count, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            for op in (ar.AR_SUM, ar.AR_MAX):
+                scale = 0.125 if (op == ar.AR_SUM and dtype != ar.AR_INT32) else 1.0
+                outs = [Guarded(count, dtype, dev) for _ in range(P)]
+                ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, dtype, op, ar.AR_ALGO_LL128, scale)
+                torch.cuda.synchronize()
+                assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                want = oracle.allreduce(sends, dtype, op, oracle.RING, scale)
+                for r in range(P):
+                    assert outs[r].guards_intact()
+                    pins.assert_bitwise(to_host(outs[r].tensor), want[r],
+                                        f"LL128 P={P} dtype={dtype} count={count} op={op} rank={r}")
+    finally:
+        ar.ar_destroy(comm)
+
+
+def test_ll_ll128_ring_interleaved(dev):
+    """LL and LL128 share the epoch counter; interleaved calls stay exact."""
+    rng = np.random.default_rng(9)
+    comm = ar.ar_init(8)
+    try:
+        for i in range(40):
+            algo = (ar.AR_ALGO_LL, ar.AR_ALGO_LL128, ar.AR_ALGO_RING)[i % 3]
+            limit = 16384 if algo == ar.AR_ALGO_LL else 262144
+            count = int(rng.integers(1, limit + 1))
+            sends = pins.random_inputs(rng, 8, count, ar.AR_FLOAT32)
+            xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+            ys = [torch.empty_like(x) for x in xs]
+            ar.ar_allreduce(comm, xs, ys, count, ar.AR_FLOAT32, ar.AR_SUM, algo, 1.0)
+            torch.cuda.synchronize()
+            want = oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.RING)
+            pins.assert_bitwise(to_host(ys[i % 8]), want[i % 8], f"call {i} algo={algo} count={count}")
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+    finally:
+        ar.ar_destroy(comm)
+
+
+def test_ll128_bounded_wait_limit_and_capture(dev):
+    comm = ar.ar_init(8)
+    try:
+        rng = np.random.default_rng(4)
+        sends = pins.random_inputs(rng, 8, 5000, ar.AR_FLOAT32)
+        xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+        ys = [torch.zeros_like(x) for x in xs]
+        # no line is ever published: every flag wait runs out and reports
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SPIN_LIMIT, 2000)
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SKIP_PRODUCER, 1)
+        ar.ar_allreduce(comm, xs, ys, 5000, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_LL128, 1.0)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_ERR_TIMEOUT
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SKIP_PRODUCER, 0)
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SPIN_LIMIT, 1 << 22)
+        ar.ar_allreduce(comm, xs, ys, 5000, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_LL128, 1.0)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        pins.assert_bitwise(to_host(ys[2]), oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.RING)[2],
+                            "LL128 after a timed-out call")
+        # above the limit, and a lowered limit
+        big = [torch.zeros(262145, device=dev) for _ in range(8)]
+        with pytest.raises(ar.ArError) as e:
+            ar.ar_allreduce(comm, big, big, 262145, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_LL128, 1.0)
+        assert e.value.status == ar.AR_ERR_UNSUPPORTED
+        ar.ar_set_option(comm, ar.AR_OPT_LL128_MAX_BYTES, 4096)
+        with pytest.raises(ar.ArError):
+            ar.ar_allreduce(comm, xs, ys, 5000, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_LL128, 1.0)
+        # not capturable: refused while a stream captures
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                with pytest.raises(ar.ArError) as e:
+                    ar.ar_allreduce(comm, xs, ys, 500, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_LL128, 1.0)
+                assert e.value.status == ar.AR_ERR_UNSUPPORTED
+                ar.ar_allreduce(comm, xs, ys, 500, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 1.0)
+        g.replay()
+        torch.cuda.synchronize()
+        pins.assert_bitwise(to_host(ys[1])[:500],
+                            oracle.allreduce([a[:500] for a in sends], ar.AR_FLOAT32, oracle.SUM, oracle.RING)[1],
+                            "ring call replayed from the capture")
+    finally:
+        ar.ar_destroy(comm)

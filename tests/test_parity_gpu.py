@@ -25,8 +25,10 @@ from gpu_util import (TORCH, VEC, Guarded, all_ranks_identical, check_sampled, d
 pytestmark = pytest.mark.gpu
 
 OPS = (ar.AR_SUM, ar.AR_MIN, ar.AR_MAX)
-ALGOS = (ar.AR_ALGO_RING, ar.AR_ALGO_TREE, ar.AR_ALGO_LL)
-ORACLE_ALGO = {ar.AR_ALGO_RING: oracle.RING, ar.AR_ALGO_TREE: oracle.TREE, ar.AR_ALGO_LL: oracle.LL}
+ALGOS = (ar.AR_ALGO_RING, ar.AR_ALGO_TREE, ar.AR_ALGO_LL, ar.AR_ALGO_LL128)
+# LL and LL128 are transports: they fold in the ring order
+ORACLE_ALGO = {ar.AR_ALGO_RING: oracle.RING, ar.AR_ALGO_TREE: oracle.TREE, ar.AR_ALGO_LL: oracle.LL,
+               ar.AR_ALGO_LL128: oracle.RING}
 
 
 @pytest.fixture(scope="module")
