@@ -46,6 +46,9 @@ PROFILES = {
     "p72_4MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll.cu"], 1.0),
+    "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_16MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
+    "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll128.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32": ("pipelined_reduce_scatter_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
@@ -72,6 +75,10 @@ WORKLOADS = {
                                     dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
     "p72_4MiB_int32_max_tree": dict(P=72, count=1024 * 1024, kind="int", sigma=1.0,
                                     dtype="i32", op="max", algo="tree", scale=1.0, seed=0),
+    "p72_4MiB_fp32_sum_hier": dict(P=72, count=1024 * 1024, kind="normal", sigma=1e-3,
+                                   dtype="f32", op="sum", algo="hier", scale=1.0 / 72, seed=3, group=8),
+    "p8_512KiB_fp32_ll128": dict(P=8, count=128 * 1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
+                                 algo="ll128", scale=1.0, seed=0),
     "p8_4KiB_fp32_ll": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
                             algo="ll", scale=1.0, seed=0),
     # the ring's two halves as standalone collectives: count = elements per shard
@@ -270,7 +277,8 @@ def oracle_throughput(w: dict, host_sends, seconds: float):
     coll = w.get("coll", "allreduce")
     dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
     op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
-    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL, "hier": None}[w["algo"]]
+    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL, "ll128": oracle.RING,
+            "hier": None}[w["algo"]]
     nccl_bytes = sizes_of(w)[2]
     if coll == "allreduce" and algo is not None:
         recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
@@ -307,7 +315,7 @@ def reference_arm(args, w, name):
     P, count = w["P"], w["count"]
     dt = {"f32": oracle.F32, "bf16": oracle.BF16, "i32": oracle.I32}[w["dtype"]]
     op = {"sum": oracle.SUM, "min": oracle.MIN, "max": oracle.MAX}[w["op"]]
-    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL}[w["algo"]]
+    algo = {"ring": oracle.RING, "tree": oracle.TREE, "ll": oracle.LL, "ll128": oracle.RING}[w["algo"]]
     # calibrate, then size the per-step slice so that warmup + steps take ~60 s
     probe = min(count, 32768)
     idx = np.arange(probe)
