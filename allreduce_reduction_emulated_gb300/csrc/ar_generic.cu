@@ -5,12 +5,13 @@
 // and the fold order needs a dynamic rank index.  Each thread owns one column
 // (one 16-byte vector of every rank) and streams it through a small ring of
 // shared-memory slots in exactly the order the fold consumes it: the ring's
-// rotated rank sequence, or the tree's postorder leaf sequence.  W
+// rotated rank sequence, or the tree's preorder leaf sequence.  W
 // asynchronous copies are kept in flight (cp.async, one commit group per
 // copy); before each value is used the thread waits until its copy has landed
 // (wait_group W-1: all but the W-1 newest groups done), reads it, and refills
-// the slot freed one step earlier with the copy W pushes ahead.  The tree's
-// combines run on a small stack.  Shared memory per thread is (W+1) x 16
+// the slot freed one step earlier with the copy W pushes ahead.  The tree
+// folds its complete lowbit-4 subtrees in registers and keeps only the nodes
+// above them on a small stack.  Shared memory per thread is (W+1) x 16
 // bytes whatever P is, so occupancy stays high at P = 72 or 256.  Threads
 // never touch each other's slots, so there is no barrier in the main loop.
 #include "../../include/ar.h"
@@ -58,12 +59,68 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// The tree's nodes carry labels 1..P; a node of lowbit b has the left
+// subtree v-b+1..v-1 and the right subtree v+1..min(v+b-1, P), and its value
+// is ((own (+) left) (+) right), its inputs pushed own first (preorder).  A
+// subtree that the rank count does not truncate ("complete", 2b - 1 nodes)
+// has a shape that depends on b alone.
+
+// Complete subtree of lowbit B <= 4, expanded at compile time (registers only).
+template <int B, int DT, int OP, class Next>
+__device__ __forceinline__ Acc<DT> small_subtree(Next& next) {
+  Acc<DT> acc = next();
+  if constexpr (B > 1) {
+    fold<DT, OP>(acc, small_subtree<B / 2, DT, OP>(next));
+    fold<DT, OP>(acc, small_subtree<B / 2, DT, OP>(next));
+  }
+  return acc;
+}
+
+// Complete subtree of lowbit b (a power of two): b <= 4 directly; above, as
+// b/4 blocks of lowbit 4 in order, with the lg = log2(b) - 2 ancestors of
+// the current block on a small stack.  Before block i the ancestors whose
+// subtree starts there are pushed (lg of them for i = 0, ctz(i) after);
+// after it the block's value folds upward: into its parent's partial if it
+// is a left child (bit 0 of i clear), else completing the parent, which then
+// folds into the grandparent by bit 1, and so on.  Stack traffic is one
+// entry per 8 inputs.
+template <int DT, int OP, class Next>
+__device__ __forceinline__ Acc<DT> complete_subtree(int b, Next& next) {
+  if (b == 1) return small_subtree<1, DT, OP>(next);
+  if (b == 2) return small_subtree<2, DT, OP>(next);
+  if (b == 4) return small_subtree<4, DT, OP>(next);
+  Acc<DT> up[kStackDepth];
+  const int lg = __ffs(b) - 3;
+  int sp = 0;
+  Acc<DT> top;
+  for (int i = 0; i < b / 4; ++i) {
+    for (int k = i == 0 ? lg : __ffs(i) - 1; k > 0; --k) up[sp++] = next();
+    top = small_subtree<4, DT, OP>(next);
+    for (int bits = i;; bits >>= 1) {
+      Acc<DT> parent = up[sp - 1];
+      fold<DT, OP>(parent, top);
+      if ((bits & 1) == 0) {  // a left child: the parent waits for its right
+        up[sp - 1] = parent;
+        break;
+      }
+      top = parent;
+      if (--sp == 0) break;   // the subtree's root is complete
+    }
+  }
+  return top;
+}
+
 // Folds the column in the algorithm's order; next() yields the widened
-// input of the next rank in the push sequence.  The tree runs as P pushes,
-// push j followed by ncomb[j] combines (the postorder program regrouped).
-// The hierarchical order folds each group's Q values, then the G partials.
+// input of the next rank in the push sequence.  The hierarchical order folds
+// each group's Q values, then the G partials.  The tree is walked along its
+// right spine from the root (the largest power of two <= P), the only part
+// the rank count truncates: at a spine node v of lowbit b either the whole
+// subtree fits (v + b - 1 <= P) and is one complete subtree, or the node's
+// partial (own (+) its complete left subtree) is kept and the walk moves to
+// the right child v + h (h the largest power of two <= P - v, below b); the
+// partials then fold bottom-up.
 template <int DT, int OP, int ALGO, class Next>
-__device__ __forceinline__ Acc<DT> fold_sequence(int P, int Q, const int16_t* ncomb, Next& next) {
+__device__ __forceinline__ Acc<DT> fold_sequence(int P, int Q, Next& next) {
   if constexpr (ALGO == kRing) {
     Acc<DT> acc = next();
     for (int k = 1; k < P; ++k) fold<DT, OP>(acc, next());
@@ -78,22 +135,35 @@ __device__ __forceinline__ Acc<DT> fold_sequence(int P, int Q, const int16_t* nc
     }
     return total;
   } else {
-    // the stack's top entry lives in registers; only deeper entries go to
-    // the (local-memory) array: a push stores the old top, a combine loads
-    // the entry below and folds the top into it
-    Acc<DT> stack[kStackDepth];
-    Acc<DT> top = next();  // push 0 (never followed by a combine)
-    int sp = 0;            // entries below the top
-    for (int j = 1; j < P; ++j) {
-      stack[sp++] = top;
-      top = next();
-      for (int c = ncomb[j]; c > 0; --c) {
-        Acc<DT> below = stack[--sp];
-        fold<DT, OP>(below, top);
-        top = below;
+    Acc<DT> spine[kStackDepth];  // partials of the spine nodes above
+    int depth = 0;
+    int v = 1;
+    while (v * 2 <= P) v *= 2;
+    int b = v;
+    Acc<DT> val;
+    for (;;) {
+      if (v + b - 1 <= P) {
+        val = complete_subtree<DT, OP>(b, next);
+        break;
       }
+      Acc<DT> own = next();
+      fold<DT, OP>(own, complete_subtree<DT, OP>(b / 2, next));
+      int h = b / 2;
+      while (h >= 1 && v + h > P) h /= 2;
+      if (h < 1) {  // no right child
+        val = own;
+        break;
+      }
+      spine[depth++] = own;
+      v += h;
+      b = h;
     }
-    return top;
+    while (depth > 0) {
+      Acc<DT> parent = spine[--depth];
+      fold<DT, OP>(parent, val);
+      val = parent;
+    }
+    return val;
   }
 }
 
@@ -128,7 +198,6 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
   __shared__ uint4* s_recv[AR_MAX_RANKS];
   __shared__ int16_t s_prog[2][kMaxProg];   // tree programs
   __shared__ int16_t s_push[2][AR_MAX_RANKS];   // tree leaf (push) sequences
-  __shared__ int16_t s_ncomb[2][AR_MAX_RANKS];  // combines after each push
   const int P = p.P;
   const int tid = threadIdx.x;
   for (int r = tid; r < P; r += kThreads) {
@@ -141,15 +210,9 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     }
     __syncthreads();
     if (tid < 2) {  // leaf order = the program's pushes in order
-      int j = -1;
-      for (int i = 0; i < p.prog_len; ++i) {
-        if (s_prog[tid][i] >= 0) {
-          s_push[tid][++j] = s_prog[tid][i];
-          s_ncomb[tid][j] = 0;
-        } else {
-          ++s_ncomb[tid][j];
-        }
-      }
+      int j = 0;
+      for (int i = 0; i < p.prog_len; ++i)
+        if (s_prog[tid][i] >= 0) s_push[tid][j++] = s_prog[tid][i];
     }
   }
   __syncthreads();
@@ -160,7 +223,6 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
        v += (uint64_t)gridDim.x * kThreads) {
     const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
     const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
-    const int16_t* ncomb = s_ncomb[t];
     RankCursor<ALGO> cur;
     cur.P = P;
     cur.push = s_push[t];
@@ -207,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
         wr = wr + 1 == kSlots ? 0 : wr + 1;
         return widen<DT>(raw);
       };
-      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
+      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, next);
       cp_async_wait<0>();
       const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
       if constexpr (SCATTER) {
@@ -218,7 +280,7 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
     } else {
       // the trailing partial vector: element-wise loads, same order
       auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[cur.next()] + n, p.tail)); };
-      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, ncomb, next);
+      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, next);
       const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
       for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
     }
