@@ -496,7 +496,16 @@ ar_status_t ar_reduce_scatter(ar_comm_t c, const void* const* sendbufs, void* co
   call.op = op;
   call.scale = scale;
   ar::LaunchInfo info;
-  cudaError_t e = vec ? ar::launch_reduce_scatter_vec(call, &info) : ar::launch_reduce_scatter_elem(call, &info);
+  cudaError_t e;
+  if (!vec) {
+    e = ar::launch_reduce_scatter_elem(call, &info);
+  } else if (c->P <= ar::kMaxStaticRanks) {  // rank-specialised, shard-owner stores
+    e = dtype == AR_FLOAT32    ? ar::launch_static_f32(call, &info)
+        : dtype == AR_BFLOAT16 ? ar::launch_static_bf16(call, &info)
+                               : ar::launch_static_i32(call, &info);
+  } else {
+    e = ar::launch_reduce_scatter_vec(call, &info);
+  }
   if (c->debug)
     std::fprintf(stderr, "[ar] reduce_scatter P=%d recvcount=%zu dtype=%s op=%s kernel=%s grid=%d status=%s\n",
                  c->P, recvcount, dtype_name(dtype), op_name(op), info.kernel, info.grid,

@@ -52,6 +52,8 @@ struct LaunchInfo {
 inline int vec_elems(int dtype) { return dtype == 1 ? 8 : 4; }
 inline size_t elem_bytes(int dtype) { return dtype == 1 ? 2 : 4; }
 
+// rank-specialised kernels (P <= kMaxStaticRanks): all-reduce, or the ring
+// reduce-scatter when c.shard != 0 (shards of whole 16-byte vectors)
 cudaError_t launch_static_f32(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
@@ -60,7 +62,7 @@ cudaError_t launch_ll(const Call& c, LaunchInfo* info);
 // LL128: 128-byte lines of 120 payload bytes + a flag word (staging, stage_stride)
 cudaError_t launch_ll128(const Call& c, LaunchInfo* info);
 size_t ll128_stage_words(size_t bytes_per_rank);
-// reduce-scatter with shards of whole 16-byte vectors (pipelined ring kernel)
+// reduce-scatter with shards of whole 16-byte vectors, any P (pipelined ring kernel)
 cudaError_t launch_reduce_scatter_vec(const Call& c, LaunchInfo* info);
 // reduce-scatter of any shard length, element by element (same order)
 cudaError_t launch_reduce_scatter_elem(const Call& c, LaunchInfo* info);

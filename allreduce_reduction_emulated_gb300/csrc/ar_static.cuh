@@ -8,7 +8,9 @@
 // result vector to all NP receive buffers.  The ring and tree "steps" are a
 // combination order here, not data movement: every input byte is read once
 // and every output byte written once, the minimum 2 * NP * count * size
-// bytes of HBM traffic.
+// bytes of HBM traffic.  The reduce-scatter variant (SCATTER) folds the same
+// ring order (shard c = chunk c, from rank c) and stores each result vector
+// only to its shard's owner: NP * count reads, count writes.
 #pragma once
 
 #include "ar_device.cuh"
@@ -76,19 +78,25 @@ __device__ __forceinline__ Acc<DT> tree_node(const uint4 (&r)[NP]) {
   return acc;
 }
 
+// Ring chunk of vector v (chunks of split vectors), 32-bit division when it fits.
+__device__ __forceinline__ int chunk_of(uint64_t v, uint64_t split) {
+  return (v < 0xffffffffull && split < 0xffffffffull) ? (int)((uint32_t)v / (uint32_t)split)
+                                                      : (int)(v / split);
+}
+
 template <int NP, int DT, int OP, int ALGO>
 __device__ __forceinline__ Acc<DT> reduce_vec(const uint4 (&r)[NP], uint64_t v, uint64_t split) {
   if constexpr (ALGO == kRing) {
-    const int c = (v < 0xffffffffull && split < 0xffffffffull) ? (int)((uint32_t)v / (uint32_t)split)
-                                                                : (int)(v / split);
-    return ring_fold<NP, DT, OP>(r, c);
+    return ring_fold<NP, DT, OP>(r, chunk_of(v, split));
   } else {
     if (v < split) return tree_node<NP, DT, OP, 0, tree_root(NP)>(r);
     return tree_node<NP, DT, OP, 1, tree_root(NP)>(r);
   }
 }
 
-template <int NP, int DT, int OP, int ALGO>
+// SCATTER (ring only): recv[c] is shard c's owner buffer, written at the
+// shard-relative position; there is no partial trailing vector.
+template <int NP, int DT, int OP, int ALGO, bool SCATTER = false>
 __global__ void __launch_bounds__(kStaticThreads)
     static_allreduce_kernel(const __grid_constant__ StaticParams<NP> p) {
   constexpr int U = kStaticUnroll;
@@ -109,14 +117,20 @@ __global__ void __launch_bounds__(kStaticThreads)
     for (int u = 0; u < U; ++u) {
       const uint64_t v = base + (uint64_t)u * kStaticThreads;
       if (v < n) {
-        const uint4 o =
-            narrow<DT>(reduce_vec<NP, DT, OP, ALGO>(r[u], v, p.split), p.scale, p.do_scale != 0);
+        if constexpr (SCATTER) {
+          const int c = chunk_of(v, p.split);
+          const uint4 o = narrow<DT>(ring_fold<NP, DT, OP>(r[u], c), p.scale, p.do_scale != 0);
+          st_stream(p.recv[c] + (v - (uint64_t)c * p.split), o);
+        } else {
+          const uint4 o =
+              narrow<DT>(reduce_vec<NP, DT, OP, ALGO>(r[u], v, p.split), p.scale, p.do_scale != 0);
 #pragma unroll
-        for (int k = 0; k < NP; ++k) st_stream(p.recv[k] + v, o);
+          for (int k = 0; k < NP; ++k) st_stream(p.recv[k] + v, o);
+        }
       }
     }
   }
-  if (p.tail != 0 && blockIdx.x == 0 && threadIdx.x == 0) {
+  if (!SCATTER && p.tail != 0 && blockIdx.x == 0 && threadIdx.x == 0) {
     uint4 r[NP];
 #pragma unroll
     for (int k = 0; k < NP; ++k) r[k] = load_partial<DT>(p.send[k] + n, p.tail);
@@ -127,10 +141,10 @@ __global__ void __launch_bounds__(kStaticThreads)
   }
 }
 
-template <int DT, int NP, int OP, int ALGO>
+template <int DT, int NP, int OP, int ALGO, bool SCATTER = false>
 cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
   constexpr int U = kStaticUnroll;
-  auto kernel = static_allreduce_kernel<NP, DT, OP, ALGO>;
+  auto kernel = static_allreduce_kernel<NP, DT, OP, ALGO, SCATTER>;
   StaticParams<NP> p;
   for (int k = 0; k < NP; ++k) {
     p.send[k] = static_cast<const uint4*>(c.send[k]);
@@ -140,6 +154,11 @@ cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
   p.nfull = c.count / V;
   p.tail = (int)(c.count % V);
   p.split = ALGO == kRing ? ring_chunk_vectors(c.count, NP, DT) : tree_split_vectors(c.count, DT);
+  if constexpr (SCATTER) {
+    if (c.shard % V != 0 || c.count != (size_t)NP * c.shard) return cudaErrorInvalidValue;
+    p.split = c.shard / V;  // whole vectors per shard
+    p.tail = 0;
+  }
   p.scale = c.scale;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   static const int blocks_per_sm = [&] {
@@ -153,7 +172,7 @@ cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
   if (c.max_blocks > 0 && (uint64_t)c.max_blocks < cap) cap = (uint64_t)c.max_blocks;
   const int grid = (int)(need < 1 ? 1 : (need < cap ? need : cap));
   kernel<<<grid, kStaticThreads, 0, c.stream>>>(p);
-  info->kernel = ALGO == kRing ? "static_ring" : "static_tree";
+  info->kernel = SCATTER ? "static_reduce_scatter" : ALGO == kRing ? "static_ring" : "static_tree";
   info->grid = grid;
   info->block = kStaticThreads;
   info->smem = 0;
@@ -162,6 +181,14 @@ cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
 
 template <int DT, int NP>
 cudaError_t launch_static_np(const Call& c, LaunchInfo* info) {
+  if (c.shard != 0) {  // reduce-scatter
+    switch (c.op) {
+      case kSum: return launch_static_one<DT, NP, kSum, kRing, true>(c, info);
+      case kMin: return launch_static_one<DT, NP, kMin, kRing, true>(c, info);
+      case kMax: return launch_static_one<DT, NP, kMax, kRing, true>(c, info);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   const int key = c.op * 4 + c.algo;
   switch (key) {
     case kSum * 4 + kRing: return launch_static_one<DT, NP, kSum, kRing>(c, info);

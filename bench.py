@@ -49,7 +49,8 @@ PROFILES = {
     "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_16MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll128.cu"], 1.0),
-    "p8_rs_8MiB_shards_fp32": ("pipelined_reduce_scatter_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p8_rs_8MiB_shards_fp32": ("static_reduce_scatter_p8_8MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
+    "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
 
@@ -86,6 +87,9 @@ WORKLOADS = {
                                    op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter"),
     "p8_ag_8MiB_shards_fp32": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                    op="sum", algo="ring", scale=1.0, seed=0, coll="all_gather"),
+    # reduce-scatter above the rank-specialised limit: 72 shards of 256 KiB (18 MiB per rank)
+    "p72_rs_256KiB_shards_fp32": dict(P=72, count=64 * 1024, kind="normal", sigma=1e-3, dtype="f32",
+                                      op="sum", algo="ring", scale=1.0 / 72, seed=0, coll="reduce_scatter"),
 }
 
 
