@@ -21,11 +21,12 @@ struct ar_comm {
   size_t stage_stride = 0;
   size_t ll_capacity_bytes = 0;  // per rank, fixed at ar_init
   size_t ll_max_bytes = 0;       // current AUTO threshold / LL limit (<= capacity)
-  uint32_t epoch = 0;            // last epoch used; 0 never appears in a staged word
   uint32_t spin_limit = 0;
   int skip_produce = 0;
   int debug = 0;
-  int* status = nullptr;         // device ar_status_t word
+  // device control block (kControlInts ints): [0] the ar_status_t word,
+  // [2..3] LL epoch state, [4..5] LL128 epoch state ({last epoch, finished blocks})
+  int* status = nullptr;
   int16_t* tree_prog = nullptr;  // device: tree 0 program then tree 1 program
   int prog_len = 0;
   // LL128 staging: P slots of `ll128_stride` 8-byte words (128-byte lines)
@@ -44,6 +45,8 @@ struct ar_comm {
 
 namespace {
 
+constexpr int kControlInts = 8;
+constexpr int kLLEpoch = 2, kLL128Epoch = 4;
 constexpr size_t kDefaultLLBytes = 65536;
 constexpr uint32_t kDefaultSpinLimit = 1u << 22;  // ~1 s of L2 polls at worst
 constexpr size_t kMaxLLBytes = 1u << 20;
@@ -219,7 +222,8 @@ ar::Call base_call(ar_comm_t c, void* stream) {
   call.status = c->status;
   call.spin_limit = c->spin_limit;
   call.skip_produce = c->skip_produce;
-  call.epoch = 0;
+  call.epoch_state = nullptr;
+  call.stage_words = 0;
   call.shard = 0;
   call.group = c->hier_group;
   call.max_blocks = c->max_blocks;
@@ -286,10 +290,10 @@ ar_status_t ar_init(int nranks, ar_comm_t* out) {
   cudaError_t e = cudaMalloc(&c->staging, stage_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&c->staging128, stage128_bytes);
   if (e == cudaSuccess) e = cudaMemset(c->staging128, 0, stage128_bytes);
-  if (e == cudaSuccess) e = cudaMalloc(&c->status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&c->status, kControlInts * sizeof(int));
   if (e == cudaSuccess) e = cudaMalloc(&c->tree_prog, prog.size() * sizeof(int16_t));
   if (e == cudaSuccess) e = cudaMemset(c->staging, 0, stage_bytes);
-  if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->status, 0, kControlInts * sizeof(int));
   if (e == cudaSuccess)
     e = cudaMemcpy(c->tree_prog, prog.data(), prog.size() * sizeof(int16_t), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
@@ -359,6 +363,16 @@ ar_status_t ar_set_option(ar_comm_t c, ar_option_t option, long long value) {
       if (value < 1 || value > c->P || c->P % value != 0) return AR_ERR_INVALID_ARG;
       c->hier_group = (int)value;
       return AR_SUCCESS;
+    case AR_OPT_LL_EPOCH: {
+      if (value < 0 || value >= 0xffffffffll) return AR_ERR_INVALID_ARG;  // see ll_epoch_begin
+      const unsigned int st[2] = {(unsigned int)value, 0u};
+      if (cudaMemcpy(c->status + kLLEpoch, st, sizeof(st), cudaMemcpyHostToDevice) != cudaSuccess ||
+          cudaMemcpy(c->status + kLL128Epoch, st, sizeof(st), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return AR_ERR_CUDA;
+      }
+      return AR_SUCCESS;
+    }
     default:
       return AR_ERR_INVALID_ARG;
   }
@@ -391,21 +405,6 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   if (chosen == AR_ALGO_LL && count * esize > c->ll_max_bytes) return AR_ERR_UNSUPPORTED;
   if (chosen == AR_ALGO_LL128 && count * esize > c->ll128_max_bytes) return AR_ERR_UNSUPPORTED;
   if (chosen == AR_ALGO_HIER && P % c->hier_group != 0) return AR_ERR_UNSUPPORTED;
-  if (chosen == AR_ALGO_LL || chosen == AR_ALGO_LL128) {
-    // The LL / LL128 epoch is a launch parameter: a captured launch would replay one
-    // epoch forever and could accept a previous replay's staged words.  Under
-    // capture AUTO takes the ring (the same result bit for bit: LL folds in
-    // the ring order) and a forced LL is refused.
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess) {
-      cudaGetLastError();
-      return AR_ERR_CUDA;
-    }
-    if (cap != cudaStreamCaptureStatusNone) {
-      if (algo != AR_ALGO_AUTO) return AR_ERR_UNSUPPORTED;
-      chosen = AR_ALGO_RING;
-    }
-  }
 
   ar::Call call;
   call.P = P;
@@ -427,33 +426,22 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   call.status = c->status;
   call.spin_limit = c->spin_limit;
   call.skip_produce = c->skip_produce;
-  call.epoch = 0;
+  call.epoch_state = nullptr;
+  call.stage_words = 0;
   call.shard = 0;
 
   ar::LaunchInfo info;
   cudaError_t e;
-  if (chosen == AR_ALGO_LL || chosen == AR_ALGO_LL128) {
-    if (c->epoch == 0xffffffffu) {
-      // every flag value has been used once: clear both staging areas and restart
-      e = cudaMemsetAsync(c->staging, 0, (size_t)P * c->stage_stride * sizeof(unsigned long long),
-                          call.stream);
-      if (e == cudaSuccess)
-        e = cudaMemsetAsync(c->staging128, 0, (size_t)P * c->ll128_stride * sizeof(unsigned long long),
-                            call.stream);
-      if (e != cudaSuccess) {
-        cudaGetLastError();
-        return AR_ERR_CUDA;
-      }
-      c->epoch = 0;
-    }
-    call.epoch = ++c->epoch;
-    if (chosen == AR_ALGO_LL) {
-      e = ar::launch_ll(call, &info);
-    } else {
-      call.staging = c->staging128;
-      call.stage_stride = c->ll128_stride;
-      e = ar::launch_ll128(call, &info);
-    }
+  if (chosen == AR_ALGO_LL) {
+    call.epoch_state = reinterpret_cast<unsigned int*>(c->status + kLLEpoch);
+    call.stage_words = (size_t)P * c->stage_stride;
+    e = ar::launch_ll(call, &info);
+  } else if (chosen == AR_ALGO_LL128) {
+    call.staging = c->staging128;
+    call.stage_stride = c->ll128_stride;
+    call.epoch_state = reinterpret_cast<unsigned int*>(c->status + kLL128Epoch);
+    call.stage_words = (size_t)P * c->ll128_stride;
+    e = ar::launch_ll128(call, &info);
   } else if (chosen == AR_ALGO_HIER) {
     e = ar::launch_generic(call, &info);
   } else if (P <= ar::kMaxStaticRanks) {
@@ -466,9 +454,9 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   if (c->debug) {
     std::fprintf(stderr,
                  "[ar] P=%d count=%zu dtype=%s op=%s algo=%s->%s kernel=%s grid=%d block=%d "
-                 "smem=%zu bytes/rank=%zu epoch=%u status=%s\n",
+                 "smem=%zu bytes/rank=%zu status=%s\n",
                  P, count, dtype_name(dtype), op_name(op), algo_name(algo), algo_name(chosen),
-                 info.kernel, info.grid, info.block, info.smem, count * esize, call.epoch,
+                 info.kernel, info.grid, info.block, info.smem, count * esize,
                  cudaGetErrorString(e));
   }
   if (e != cudaSuccess) {

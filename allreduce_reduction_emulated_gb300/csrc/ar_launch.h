@@ -35,7 +35,10 @@ struct Call {
   size_t shard;
   int group;                    // hierarchical order: ranks per group
   int max_blocks;               // > 0: at most this many CTAs (grid-stride loops)
-  uint32_t epoch;
+  // LL / LL128 epoch state on the device ({last epoch, finished blocks}) and
+  // the staging words it covers (cleared when the epoch wraps)
+  unsigned int* epoch_state;
+  size_t stage_words;
   uint32_t spin_limit;
   int skip_produce;
 };

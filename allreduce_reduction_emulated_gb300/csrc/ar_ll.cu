@@ -12,10 +12,12 @@
 //            their flags equal the epoch, folds the payloads in ring order
 //            (x_g, x_{g+1}, ...) -- so LL == RING bit for bit -- and writes
 //            the result straight into all P receive buffers (the all-gather).
-// A new epoch per call means the staging area is never cleared between calls.
-// All blocks must be resident at once (a reducer waits for other blocks), so
-// the kernel is launched cooperatively; every flag wait is bounded, and on
-// its limit the thread records AR_ERR_TIMEOUT in the status word and exits.
+// A new epoch per call means the staging area is never cleared between calls;
+// the epoch is kept on the device (ll_epoch_begin / ll_epoch_end), so a call
+// can be captured in a CUDA graph.  All blocks must be resident at once (a
+// reducer waits for other blocks), so the kernel is launched cooperatively;
+// every flag wait is bounded, and on its limit the thread records
+// AR_ERR_TIMEOUT in the status word and stops reducing.
 #include "../../include/ar.h"
 #include "ar_device.cuh"
 #include "ar_launch.h"
@@ -41,7 +43,8 @@ struct LLParams {
   uint64_t nbytes;       // bytes per rank
   uint64_t nwords;       // 4-byte payload words per rank
   uint64_t chunk_words;  // words per ring chunk
-  uint32_t epoch;
+  unsigned int* epoch_state;
+  uint64_t stage_words;  // whole staging area (P slots), cleared on epoch wrap
   uint32_t spin_limit;
   int P;
   int bpr;               // blocks per rank group
@@ -96,22 +99,12 @@ __device__ __forceinline__ void store_payload(void* buf, uint64_t w, uint64_t nb
   else static_cast<uint16_t*>(buf)[2 * w] = (uint16_t)v;
 }
 
+// Reduces ring chunk g in ring order and writes it to every rank; returns
+// early (status AR_ERR_TIMEOUT) if a flag wait runs out.
 template <int MAXP, int DT, int OP>
-__global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_constant__ LLParams<MAXP> p) {
+__device__ __forceinline__ void ll_reduce_chunk(const LLParams<MAXP>& p, int g, uint64_t lt, uint64_t nt,
+                                                uint32_t epoch) {
   const int P = p.P;
-  const int g = blockIdx.x / p.bpr;
-  const uint64_t lt = (uint64_t)(blockIdx.x % p.bpr) * kLLThreads + threadIdx.x;
-  const uint64_t nt = (uint64_t)p.bpr * kLLThreads;
-  const unsigned long long tag = (unsigned long long)p.epoch << 32;
-
-  // produce: stage rank g's payload words with this call's flag
-  if (!p.skip_produce) {
-    unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
-    for (uint64_t w = lt; w < p.nwords; w += nt)
-      st_relaxed_u64(slot + w, tag | load_payload(p.send[g], w, p.nbytes));
-  }
-
-  // reduce chunk g in ring order and write it to every rank
   const uint64_t w0 = (uint64_t)g * p.chunk_words;
   uint64_t w1 = w0 + p.chunk_words;
   if (w1 > p.nwords) w1 = p.nwords;
@@ -132,7 +125,7 @@ __global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_c
       for (int j = 0; j < kLLBatch; ++j) {
         const int k = k0 + j;
         if (k >= P) break;
-        if ((uint32_t)(x[j] >> 32) != p.epoch) {
+        if ((uint32_t)(x[j] >> 32) != epoch) {
           int r = g + k;
           if (r >= P) r -= P;
           const unsigned long long* src = p.staging + (uint64_t)r * p.stride + w;
@@ -143,7 +136,7 @@ __global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_c
               return;
             }
             x[j] = ld_relaxed_u64(src);
-          } while ((uint32_t)(x[j] >> 32) != p.epoch);
+          } while ((uint32_t)(x[j] >> 32) != epoch);
         }
         const Word<DT> xw = widen_word<DT>((uint32_t)x[j]);
         if (k == 0) acc = xw;
@@ -153,6 +146,24 @@ __global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_c
     const uint32_t out = narrow_word<DT>(acc, p.scale, p.do_scale != 0);
     for (int r = 0; r < P; ++r) store_payload(p.recv[r], w, p.nbytes, out);
   }
+}
+
+template <int MAXP, int DT, int OP>
+__global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_constant__ LLParams<MAXP> p) {
+  const int g = blockIdx.x / p.bpr;
+  const uint64_t lt = (uint64_t)(blockIdx.x % p.bpr) * kLLThreads + threadIdx.x;
+  const uint64_t nt = (uint64_t)p.bpr * kLLThreads;
+  const uint32_t epoch = ll_epoch_begin(p.epoch_state);
+  const unsigned long long tag = (unsigned long long)epoch << 32;
+
+  // produce: stage rank g's payload words with this call's flag
+  if (!p.skip_produce) {
+    unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
+    for (uint64_t w = lt; w < p.nwords; w += nt)
+      st_relaxed_u64(slot + w, tag | load_payload(p.send[g], w, p.nbytes));
+  }
+  ll_reduce_chunk<MAXP, DT, OP>(p, g, lt, nt, epoch);
+  ll_epoch_end(p.epoch_state, epoch, p.staging, p.stage_words);
 }
 
 template <int MAXP, int DT, int OP>
@@ -169,7 +180,8 @@ cudaError_t launch_ll_one(const Call& c, LaunchInfo* info) {
   p.nbytes = c.count * elem_bytes(DT);
   p.nwords = (p.nbytes + 3) / 4;
   p.chunk_words = ring_chunk_vectors(c.count, c.P, DT) * 4;  // 16-byte vectors = 4 words
-  p.epoch = c.epoch;
+  p.epoch_state = c.epoch_state;
+  p.stage_words = c.stage_words;
   p.spin_limit = c.spin_limit;
   p.P = c.P;
   p.skip_produce = c.skip_produce;

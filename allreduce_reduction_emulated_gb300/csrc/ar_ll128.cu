@@ -11,7 +11,9 @@
 // the payload.  Emulated like LL inside one cooperative kernel: block group g
 // stages rank g's lines, then reduces ring chunk g in ring order (so LL128 ==
 // RING bit for bit) and writes the result into every rank's receive buffer.
-// Every flag wait is bounded; on its limit a thread records AR_ERR_TIMEOUT.
+// The epoch is kept on the device as for LL, so calls can be captured in a
+// CUDA graph.  Every flag wait is bounded; on its limit a thread records
+// AR_ERR_TIMEOUT and stops reducing.
 #include "../../include/ar.h"
 #include "ar_device.cuh"
 #include "ar_launch.h"
@@ -36,7 +38,8 @@ struct LL128Params {
   uint64_t nwords;       // 8-byte payload words per rank
   uint64_t nlines;       // lines per rank
   uint64_t chunk_words;  // payload words per ring chunk (16-byte chunks: even)
-  uint32_t epoch;
+  unsigned int* epoch_state;
+  uint64_t stage_words;  // whole staging area (P slots), cleared on epoch wrap
   uint32_t spin_limit;
   int P;
   int bpr;
@@ -118,39 +121,13 @@ __device__ __forceinline__ unsigned long long narrow8(Word8<DT> a, float scale, 
   }
 }
 
+// Reduces ring chunk g, one 8-byte payload word per thread per step, and
+// writes it to every rank; returns early (status AR_ERR_TIMEOUT) if a flag
+// wait runs out.
 template <int MAXP, int DT, int OP>
-__global__ void __launch_bounds__(kThreads) ll128_allreduce_kernel(const __grid_constant__ LL128Params<MAXP> p) {
+__device__ __forceinline__ void ll128_reduce_chunk(const LL128Params<MAXP>& p, int g,
+                                                   unsigned long long flag) {
   const int P = p.P;
-  const int g = blockIdx.x / p.bpr;
-  const int lane = threadIdx.x & 31;
-  const unsigned long long flag = (unsigned long long)p.epoch;
-
-  // produce: a warp writes 4 lines at a time, 8 lanes per line (16 bytes
-  // each); lane 7 of each line then publishes the line with its flag word
-  if (!p.skip_produce) {
-    unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
-    const uint64_t warps = (uint64_t)p.bpr * (kThreads / 32);
-    const uint64_t warp = (uint64_t)(blockIdx.x % p.bpr) * (kThreads / 32) + threadIdx.x / 32;
-    const int part = lane & 7;  // 16-byte part of the line
-    for (uint64_t base = warp * 4; base < p.nlines; base += warps * 4) {
-      const uint64_t line = base + (uint64_t)(lane >> 3);
-      const bool live = line < p.nlines;
-      const uint64_t w0 = line * kPayloadWords + 2 * part;  // payload words of this part
-      if (live) {
-        slot[line * kLineWords + 2 * part] = w0 < p.nwords ? load_word8(p.send[g], w0, p.nbytes) : 0ull;
-        if (part < 7)
-          slot[line * kLineWords + 2 * part + 1] =
-              w0 + 1 < p.nwords ? load_word8(p.send[g], w0 + 1, p.nbytes) : 0ull;
-      }
-      __threadfence();  // each lane's payload words before the warp barrier ...
-      __syncwarp();
-      // ... and the flag after it, with release: a reader that acquires the
-      // flag sees the whole line
-      if (live && part == 7) st_release_u64(slot + line * kLineWords + kPayloadWords, flag);
-    }
-  }
-
-  // reduce ring chunk g: one 8-byte payload word per thread per step
   const uint64_t lt = (uint64_t)(blockIdx.x % p.bpr) * kThreads + threadIdx.x;
   const uint64_t nt = (uint64_t)p.bpr * kThreads;
   const uint64_t w0 = (uint64_t)g * p.chunk_words;
@@ -197,6 +174,42 @@ __global__ void __launch_bounds__(kThreads) ll128_allreduce_kernel(const __grid_
 }
 
 template <int MAXP, int DT, int OP>
+__global__ void __launch_bounds__(kThreads) ll128_allreduce_kernel(const __grid_constant__ LL128Params<MAXP> p) {
+  const int g = blockIdx.x / p.bpr;
+  const int lane = threadIdx.x & 31;
+  const uint32_t epoch = ll_epoch_begin(p.epoch_state);
+  const unsigned long long flag = (unsigned long long)epoch;
+
+  // produce: a warp writes 4 lines at a time, 8 lanes per line (16 bytes
+  // each); lane 7 of each line then publishes the line with its flag word
+  if (!p.skip_produce) {
+    unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
+    const uint64_t warps = (uint64_t)p.bpr * (kThreads / 32);
+    const uint64_t warp = (uint64_t)(blockIdx.x % p.bpr) * (kThreads / 32) + threadIdx.x / 32;
+    const int part = lane & 7;  // 16-byte part of the line
+    for (uint64_t base = warp * 4; base < p.nlines; base += warps * 4) {
+      const uint64_t line = base + (uint64_t)(lane >> 3);
+      const bool live = line < p.nlines;
+      const uint64_t w0 = line * kPayloadWords + 2 * part;  // payload words of this part
+      if (live) {
+        slot[line * kLineWords + 2 * part] = w0 < p.nwords ? load_word8(p.send[g], w0, p.nbytes) : 0ull;
+        if (part < 7)
+          slot[line * kLineWords + 2 * part + 1] =
+              w0 + 1 < p.nwords ? load_word8(p.send[g], w0 + 1, p.nbytes) : 0ull;
+      }
+      __threadfence();  // each lane's payload words before the warp barrier ...
+      __syncwarp();
+      // ... and the flag after it, with release: a reader that acquires the
+      // flag sees the whole line
+      if (live && part == 7) st_release_u64(slot + line * kLineWords + kPayloadWords, flag);
+    }
+  }
+
+  ll128_reduce_chunk<MAXP, DT, OP>(p, g, flag);
+  ll_epoch_end(p.epoch_state, epoch, p.staging, p.stage_words);
+}
+
+template <int MAXP, int DT, int OP>
 cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   auto kernel = ll128_allreduce_kernel<MAXP, DT, OP>;
   LL128Params<MAXP> p;
@@ -211,7 +224,8 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   p.nwords = (p.nbytes + 7) / 8;
   p.nlines = (p.nwords + kPayloadWords - 1) / kPayloadWords;
   p.chunk_words = ring_chunk_vectors(c.count, c.P, DT) * 2;  // 16-byte vectors = 2 words
-  p.epoch = c.epoch;
+  p.epoch_state = c.epoch_state;
+  p.stage_words = c.stage_words;
   p.spin_limit = c.spin_limit;
   p.P = c.P;
   p.skip_produce = c.skip_produce;

@@ -11,10 +11,10 @@
 // library holds that array (about 1 MiB) until the process exits.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents.  Each call stages its words under a fresh epoch, so stale words
-// never match; when the 32-bit epoch runs out the staging words are cleared
-// once.  The status word starts at zero (module load) and is cleared whenever
-// it is read.  Calls that overlap on the GPU (for example on two streams)
+// contents.  Each call stages its words under a fresh epoch, kept in the same
+// array on the device, so stale words never match; when the 32-bit epoch runs
+// out the kernel clears the staging words once.  The status word starts at
+// zero (module load) and is cleared whenever it is read.  Calls that overlap on the GPU (for example on two streams)
 // race on the array and must not be issued.
 #include <cstdint>
 #include <mutex>
@@ -27,7 +27,7 @@
 namespace {
 
 constexpr size_t kStride = AR_NOALLOC_MAX_BYTES / 4 + 4;  // 8-byte words per rank slot
-constexpr size_t kSlotsOffset = 32;                        // word 0 holds the status
+constexpr size_t kSlotsOffset = 32;  // word 0: the status; word 1: the epoch state
 constexpr size_t kScratchWords = kSlotsOffset + (size_t)AR_NOALLOC_MAX_RANKS * kStride;
 constexpr uint32_t kSpinLimit = 1u << 22;                  // ~1 s of polls, then AR_ERR_TIMEOUT
 constexpr int kMaxDevices = 64;
@@ -43,8 +43,6 @@ struct DeviceState {
   cudaError_t setup = cudaSuccess;
   unsigned long long* base = nullptr;  // device address of g_noalloc_scratch
   int sms = 0;
-  uint32_t epoch = 0;
-  std::mutex lock;
 };
 
 DeviceState g_state[kMaxDevices];
@@ -123,18 +121,10 @@ extern "C" ar_status_t ar_allreduce_ll_noalloc(int nranks, const void* const* se
     c.max_blocks = 0;
     c.group = 1;
     c.shard = 0;
-    cudaError_t e = cudaSuccess;
-    {
-      std::lock_guard<std::mutex> g(s.lock);
-      if (s.epoch == 0xffffffffu) {
-        // every flag value has been used: clear the staging words once
-        e = cudaMemsetAsync(c.staging, 0, (size_t)AR_NOALLOC_MAX_RANKS * kStride * 8, st);
-        s.epoch = 0;
-      }
-      c.epoch = ++s.epoch;
-    }
+    c.epoch_state = reinterpret_cast<unsigned int*>(s.base + 1);
+    c.stage_words = (size_t)AR_NOALLOC_MAX_RANKS * kStride;  // every slot, whatever P
     ar::LaunchInfo info;
-    if (e == cudaSuccess) e = ar::launch_ll(c, &info);
+    cudaError_t e = ar::launch_ll(c, &info);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return AR_ERR_CUDA;

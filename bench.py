@@ -547,6 +547,9 @@ def fit_alpha_beta(points):
     return alpha, beta
 
 
+SPIN_CYCLES = 200_000   # ~0.1 ms of GPU spin ahead of a timed small call
+
+
 def sweep(args):
     """nccl-tests style sweep ("NCCL and NVSHMEM ...", exercise 1: 8 B .. 1 GiB,
     factor 2) for AUTO and each forced algorithm, with t = alpha + beta * n."""
@@ -585,18 +588,27 @@ def sweep(args):
             for _ in range(3):
                 call()
             torch.cuda.synchronize()
+            t_issue = None
             if small:
-                times = []
+                # "us": the call's GPU time -- a spin kernel keeps the GPU busy
+                # while the host enqueues the start event and the call, so the
+                # host's issue time is not inside the events; "us_with_issue":
+                # the events bracket the host's issue of the call as well
+                times, issued = [], []
                 for _ in range(50):
-                    flush.zero_()
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    call()
-                    b.record(stream)
-                    torch.cuda.synchronize()
-                    times.append(a.elapsed_time(b))
+                    for hide, out in ((True, times), (False, issued)):
+                        flush.zero_()
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        if hide:
+                            torch.cuda._sleep(SPIN_CYCLES)
+                        a.record(stream)
+                        call()
+                        b.record(stream)
+                        torch.cuda.synchronize()
+                        out.append(a.elapsed_time(b))
                 t = statistics.median(times) * 1e-3
+                t_issue = statistics.median(issued) * 1e-3
             else:
                 iters = max(5, min(200, int(2e9 / (2 * P * nbytes))))
                 a = torch.cuda.Event(enable_timing=True)
@@ -611,7 +623,8 @@ def sweep(args):
                 raise SystemExit("device status error in the sweep")
             rows.append({"bytes_per_rank": nbytes, "algo": names[algo],
                          "resolved": names[ar.ar_select_algo(comm, count, ar.AR_FLOAT32, algo)],
-                         "us": t * 1e6, "algbw": nbytes / t / 1e9,
+                         "us": t * 1e6, "us_with_issue": None if t_issue is None else t_issue * 1e6,
+                         "algbw": nbytes / t / 1e9,
                          "busbw": nbytes / t / 1e9 * 2 * (P - 1) / P,
                          "hbm_gbs": 2 * P * nbytes / t / 1e9, "l2_flushed": small})
         count *= 2

@@ -138,11 +138,12 @@ ar_status_t ar_init(int nranks, ar_comm_t* out);
  * AR_ERR_UNSUPPORTED) before anything is enqueued; launch failures return
  * AR_ERR_CUDA; device-side errors (LL spin limit) are reported later by
  * ar_get_status.
- * CUDA graphs: RING, TREE and HIER calls may be captured and replayed (the
- * buffers are then fixed).  LL and LL128 calls are not capturable -- each
- * call needs a fresh epoch -- so while `stream` is capturing, AUTO resolves
- * to RING (identical result) and a forced AR_ALGO_LL / AR_ALGO_LL128 returns
- * AR_ERR_UNSUPPORTED.
+ * CUDA graphs: every algorithm may be captured and replayed (the buffers
+ * are then fixed).  The LL / LL128 epoch lives in device memory and each
+ * launch takes the next value itself, so a replayed call never matches an
+ * earlier call's staged words.  Calls on one communicator must still run one
+ * at a time on the GPU (one stream, or streams ordered by events): they share
+ * the staging areas and the epoch.
  */
 ar_status_t ar_allreduce(ar_comm_t comm, const void* const* sendbufs, void* const* recvbufs,
                          size_t count, ar_dtype_t dtype, ar_op_t op, ar_algo_t algo,
@@ -172,7 +173,8 @@ ar_status_t ar_destroy(ar_comm_t comm);
 ar_status_t ar_select_algo(ar_comm_t comm, size_t count, ar_dtype_t dtype, ar_algo_t algo,
                            ar_algo_t* chosen);
 
-/* Per-communicator options (host only; take effect on the next call). */
+/* Per-communicator options (take effect on the next call; host only except
+ * AR_OPT_LL_EPOCH). */
 typedef enum {
     AR_OPT_LL_MAX_BYTES = 0,     /* LL limit in bytes per rank, 16 .. the size given
                                     at ar_init (default 65536 or AR_LL_MAX_BYTES)       */
@@ -188,11 +190,17 @@ typedef enum {
     AR_OPT_AUTO_TUNED = 7,       /* nonzero: AUTO follows the table measured by
                                     ar_tune; 0: the fixed LL-up-to-the-limit rule
                                     (default; ar_tune sets it to 1)                  */
-    AR_OPT_MAX_BLOCKS = 5        /* > 0: ring / tree / hierarchical / reduce-scatter /
+    AR_OPT_MAX_BLOCKS = 5,       /* > 0: ring / tree / hierarchical / reduce-scatter /
                                     all-gather kernels launch at most this many
                                     thread blocks (grid-stride), leaving the other
                                     SMs to kernels on other streams; 0 = no cap
                                     (default).  Results do not change.              */
+    AR_OPT_LL_EPOCH = 8          /* test hook: sets the last epoch used by LL and
+                                    LL128 (0 .. 2^32 - 2; the next call uses
+                                    value + 1; the call that uses 2^32 - 1 clears
+                                    the staging area and restarts at 1).  Writes
+                                    device memory synchronously: synchronize the
+                                    communicator's streams first.                 */
 } ar_option_t;
 
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);

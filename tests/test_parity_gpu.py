@@ -351,14 +351,14 @@ def test_p72_int32_sum_max_min(dev, comms):
 def test_bucket_loop_captured_in_a_cuda_graph(dev, comms):
     """A DDP-style bucket loop recorded once into a CUDA graph and replayed.
 
-    Ring and tree calls replay correctly on new data written into the same
-    buffers; under capture AUTO takes the ring for a small message (LL needs
-    a fresh epoch per call) and a forced LL is refused without disturbing the
-    capture.
+    Ring, tree, AUTO (LL for the small bucket) and a forced LL128 call replay
+    correctly on new data written into the same buffers: the LL protocols
+    take their epoch from device memory, so replays never reuse one.
     """
     comm = comms(8)
-    sizes = [1 << 20, 3 * (1 << 18) + 5, 1000]          # two large buckets and a small one
-    algos = [ar.AR_ALGO_RING, ar.AR_ALGO_TREE, ar.AR_ALGO_AUTO]
+    sizes = [1 << 20, 3 * (1 << 18) + 5, 1000, 40000]   # two large buckets and two small ones
+    algos = [ar.AR_ALGO_RING, ar.AR_ALGO_TREE, ar.AR_ALGO_AUTO, ar.AR_ALGO_LL128]
+    assert ar.ar_select_algo(comm, 1000, ar.AR_FLOAT32, ar.AR_ALGO_AUTO) == ar.AR_ALGO_LL
     sends = [[torch.empty(n, device=dev) for _ in range(8)] for n in sizes]
     recvs = [[torch.empty(n, device=dev) for _ in range(8)] for n in sizes]
 
@@ -373,12 +373,8 @@ def test_bucket_loop_captured_in_a_cuda_graph(dev, comms):
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             run_all()
-            with pytest.raises(ar.ArError) as e:
-                ar.ar_allreduce(comm, sends[2], recvs[2], sizes[2], ar.AR_FLOAT32, ar.AR_SUM,
-                                ar.AR_ALGO_LL, 1.0)
-            assert e.value.status == ar.AR_ERR_UNSUPPORTED
     rng = np.random.default_rng(41)
-    for replay in range(2):
+    for replay in range(3):
         host = [pins.random_inputs(rng, 8, n, ar.AR_FLOAT32) for n in sizes]
         for b in range(len(sizes)):
             for r in range(8):
