@@ -20,6 +20,7 @@
 // AR_ERR_TIMEOUT in the status word and stops reducing.
 #include "../../include/ar.h"
 #include "ar_device.cuh"
+#include "ar_ll_epoch.cuh"
 #include "ar_launch.h"
 
 namespace ar {

@@ -16,6 +16,7 @@
 // AR_ERR_TIMEOUT and stops reducing.
 #include "../../include/ar.h"
 #include "ar_device.cuh"
+#include "ar_ll_epoch.cuh"
 #include "ar_launch.h"
 
 namespace ar {

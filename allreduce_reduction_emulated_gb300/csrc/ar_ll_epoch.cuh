@@ -1,0 +1,61 @@
+// ar_ll_epoch.cuh -- the LL / LL128 per-call epoch, kept on the device.
+//
+// The LL protocols tag each staged word with the call's epoch.  The epoch
+// lives on the device, so a call carries no host state and can be captured
+// in a CUDA graph and replayed: state[0] is the last epoch used (0: none
+// since the staging area was last cleared, and 0 is never a live flag),
+// state[1] counts the blocks of the running call that have finished.
+#pragma once
+
+#include "ar_device.cuh"
+
+namespace ar {
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(unsigned int* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Every block reads the last epoch before doing anything; this call uses
+// the next one.
+__device__ __forceinline__ uint32_t ll_epoch_begin(const unsigned int* state) {
+  __shared__ uint32_t s_epoch;
+  if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(state) + 1u;
+  __syncthreads();
+  return s_epoch;
+}
+
+// Called by every thread of every block once the block is done with the
+// staging area.  The last block to finish publishes the epoch, after every
+// block has read the old value at its start; when the last 32-bit value has
+// been used it first clears the whole staging area (`words` 8-byte words),
+// so that numbering can restart at 1 without old words matching.
+__device__ __forceinline__ void ll_epoch_end(unsigned int* state, uint32_t epoch,
+                                             unsigned long long* staging, uint64_t words) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&state[1], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const bool wrap = epoch == 0xffffffffu;
+  if (wrap) {
+    for (uint64_t i = threadIdx.x; i < words; i += blockDim.x) st_relaxed_u64(staging + i, 0ull);
+    __threadfence();
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    st_relaxed_u32(&state[1], 0u);
+    st_relaxed_u32(&state[0], wrap ? 0u : epoch);
+  }
+}
+
+}  // namespace ar

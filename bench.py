@@ -45,10 +45,10 @@ PROFILES = {
     "p72_16MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p72_4MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
-    "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll.cu"], 1.0),
+    "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll.cu"], 1.0),
     "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_16MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
-    "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll128.cu"], 1.0),
+    "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll128.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32": ("static_reduce_scatter_p8_8MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
