@@ -1,0 +1,86 @@
+"""bench.py's host logic on CPU: workload byte counts and the ncu summaries.
+
+The roofline's `achieved` divides each workload's algorithmic bytes by the
+kernel's time, and `traffic` comes from the committed ncu summary under
+profiles/ only while the kernel sources still hash to the captured value.
+"""
+import os
+import re
+
+import pytest
+
+import bench
+
+
+@pytest.mark.parametrize("name", sorted(bench.WORKLOADS))
+def test_algorithmic_bytes_follow_the_collective(name):
+    w = bench.WORKLOADS[name]
+    P, n, es = w["P"], w["count"], bench.ESIZE[w["dtype"]]
+    n_in, n_out, nccl_bytes, bus, hbm = bench.sizes_of(w)
+    coll = w.get("coll", "allreduce")
+    if coll == "allreduce":
+        # every rank's buffer read once, the result written to every rank
+        assert (n_in, n_out) == (n, n)
+        assert hbm == P * n * es + P * n * es
+        assert nccl_bytes == n * es and bus == pytest.approx(2 * (P - 1) / P)
+    elif coll == "reduce_scatter":
+        # P inputs of P shards read, one shard written per rank
+        assert (n_in, n_out) == (P * n, n)
+        assert hbm == P * (P * n) * es + P * n * es
+        assert nccl_bytes == P * n * es and bus == pytest.approx((P - 1) / P)
+    else:
+        # one shard read per rank, P shards written per rank
+        assert (n_in, n_out) == (n, P * n)
+        assert hbm == P * n * es + P * (P * n) * es
+        assert nccl_bytes == P * n * es and bus == pytest.approx((P - 1) / P)
+
+
+def test_headline_bytes_per_launch():
+    w = bench.WORKLOADS["p8_64MiB_fp32_ring_ddp_mean"]
+    assert bench.sizes_of(w)[4] == 2 * 8 * 16_777_216 * 4 == 1_073_741_824
+
+
+def test_ddp_bucket_layout():
+    # 24 x {2048x8192, 8192x2048, 2048x6144, 2048x2048} fp32 cut into 25 MiB buckets
+    assert bench.DDP_PARAMS == 1_207_959_552
+    assert bench.DDP_BUCKET == 6_553_600
+    full, rest = divmod(bench.DDP_PARAMS, bench.DDP_BUCKET)
+    assert (full, rest) == (184, 2_097_152)
+
+
+@pytest.mark.parametrize("name", sorted(bench.PROFILES))
+def test_profile_summary_is_complete(name):
+    fname, sources, scale = bench.PROFILES[name]
+    assert name in bench.WORKLOADS
+    assert scale > 0
+    for s in sources:
+        assert os.path.isfile(os.path.join(bench.ROOT, s)), s
+    path = os.path.join(bench.ROOT, "profiles", fname)
+    assert os.path.isfile(path), fname
+    text = open(path).read()
+    assert re.search(r"^dram_bytes_per_launch: \d+$", text, re.M)
+    assert re.search(r"^source_sha256: [0-9a-f]{16}$", text, re.M)
+    # the commands that made it run committed files only, with the clocks left alone
+    assert "python bench.py --workload" in text
+    for line in text.splitlines():
+        if line.strip().startswith("ncu "):
+            assert "--clock-control none" in line
+
+
+def test_the_headline_has_a_summary():
+    # other workloads without a capture of their own kernel instantiation
+    # report traffic null rather than borrow another one's counters
+    assert "p8_64MiB_fp32_ring_ddp_mean" in bench.PROFILES
+
+
+def test_traffic_only_while_the_sources_match(monkeypatch):
+    name = "p72_16MiB_int32_sum_ring"                    # a scaled (4 MiB -> 16 MiB) summary
+    fname, sources, scale = bench.PROFILES[name]
+    text = open(os.path.join(bench.ROOT, "profiles", fname)).read()
+    captured = re.search(r"^source_sha256: ([0-9a-f]{16})$", text, re.M).group(1)
+    per_launch = int(re.search(r"^dram_bytes_per_launch: (\d+)$", text, re.M).group(1))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda s: captured)
+    assert bench.profiled_traffic(name) == per_launch * scale
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda s: "0" * 16)
+    assert bench.profiled_traffic(name) is None
+    assert bench.profiled_traffic("no_such_workload") is None
