@@ -27,8 +27,7 @@ struct ar_comm {
   // device control block (kControlInts ints): [0] the ar_status_t word,
   // [2..3] LL epoch state, [4..5] LL128 epoch state ({last epoch, finished blocks})
   int* status = nullptr;
-  int16_t* tree_prog = nullptr;  // device: tree 0 program then tree 1 program
-  int prog_len = 0;
+  int16_t* tree_push = nullptr;  // device: tree 0's then tree 1's ranks in preorder (P each)
   // LL128 staging: P slots of `ll128_stride` 8-byte words (128-byte lines)
   unsigned long long* staging128 = nullptr;
   size_t ll128_stride = 0;
@@ -68,28 +67,13 @@ bool valid_algo(int a) {
          a == AR_ALGO_HIER || a == AR_ALGO_LL128;
 }
 
-// Postorder program of tree t: push own rank, then each child's subtree
-// followed by a combine -- i.e. ((own (+) left) (+) right).
-void emit_tree(int v, int P, int t, std::vector<int16_t>& out) {
+// Ranks of tree t in the order its fold consumes them: own rank, then the
+// left subtree, then the right subtree (preorder), for ((own (+) left) (+) right).
+void emit_preorder(int v, int P, int t, std::vector<int16_t>& out) {
   out.push_back((int16_t)ar::tree_owner(v, P, t));
   const int l = ar::tree_left(v), r = ar::tree_right(v, P);
-  if (l) {
-    emit_tree(l, P, t, out);
-    out.push_back(-1);
-  }
-  if (r) {
-    emit_tree(r, P, t, out);
-    out.push_back(-1);
-  }
-}
-
-int program_depth(const std::vector<int16_t>& prog) {
-  int sp = 0, depth = 0;
-  for (int16_t op : prog) {
-    sp += op >= 0 ? 1 : -1;
-    depth = std::max(depth, sp);
-  }
-  return depth;
+  if (l) emit_preorder(l, P, t, out);
+  if (r) emit_preorder(r, P, t, out);
 }
 
 const char* dtype_name(int d) { return d == AR_FLOAT32 ? "f32" : d == AR_BFLOAT16 ? "bf16" : "i32"; }
@@ -108,7 +92,7 @@ void release(ar_comm* c) {
   if (c->staging) cudaFree(c->staging);
   if (c->staging128) cudaFree(c->staging128);
   if (c->status) cudaFree(c->status);
-  if (c->tree_prog) cudaFree(c->tree_prog);
+  if (c->tree_push) cudaFree(c->tree_push);
   delete c;
 }
 
@@ -215,8 +199,7 @@ ar::Call base_call(ar_comm_t c, void* stream) {
   call.P = c->P;
   call.stream = static_cast<cudaStream_t>(stream);
   call.sms = c->sms;
-  call.tree_prog = c->tree_prog;
-  call.prog_len = c->prog_len;
+  call.tree_push = c->tree_push;
   call.staging = c->staging;
   call.stage_stride = c->stage_stride;
   call.status = c->status;
@@ -280,10 +263,9 @@ ar_status_t ar_init(int nranks, ar_comm_t* out) {
   c->ll128_max_bytes = (size_t)ll128;
   c->ll128_stride = ar::ll128_stage_words(c->ll128_capacity_bytes);
   const size_t stage128_bytes = (size_t)nranks * c->ll128_stride * sizeof(unsigned long long);
-  std::vector<int16_t> prog;
-  for (int t = 0; t < 2; ++t) emit_tree(ar::tree_root(nranks), nranks, t, prog);
-  c->prog_len = (int)prog.size() / 2;
-  if (program_depth(prog) > 16) {  // cannot happen for nranks <= AR_MAX_RANKS
+  std::vector<int16_t> push;
+  for (int t = 0; t < 2; ++t) emit_preorder(ar::tree_root(nranks), nranks, t, push);
+  if (push.size() != 2 * (size_t)nranks) {  // every rank once per tree
     delete c;
     return AR_ERR_INVALID_ARG;
   }
@@ -291,11 +273,11 @@ ar_status_t ar_init(int nranks, ar_comm_t* out) {
   if (e == cudaSuccess) e = cudaMalloc(&c->staging128, stage128_bytes);
   if (e == cudaSuccess) e = cudaMemset(c->staging128, 0, stage128_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&c->status, kControlInts * sizeof(int));
-  if (e == cudaSuccess) e = cudaMalloc(&c->tree_prog, prog.size() * sizeof(int16_t));
+  if (e == cudaSuccess) e = cudaMalloc(&c->tree_push, push.size() * sizeof(int16_t));
   if (e == cudaSuccess) e = cudaMemset(c->staging, 0, stage_bytes);
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, kControlInts * sizeof(int));
   if (e == cudaSuccess)
-    e = cudaMemcpy(c->tree_prog, prog.data(), prog.size() * sizeof(int16_t), cudaMemcpyHostToDevice);
+    e = cudaMemcpy(c->tree_push, push.data(), push.size() * sizeof(int16_t), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaGetLastError();
     release(c);
@@ -419,8 +401,7 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   call.scale = scale;
   call.stream = static_cast<cudaStream_t>(stream);
   call.sms = c->sms;
-  call.tree_prog = c->tree_prog;
-  call.prog_len = c->prog_len;
+  call.tree_push = c->tree_push;
   call.staging = c->staging;
   call.stage_stride = c->stage_stride;
   call.status = c->status;

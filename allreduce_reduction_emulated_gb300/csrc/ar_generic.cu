@@ -33,13 +33,11 @@ constexpr int kWindow = AR_GENERIC_WINDOW;    // copies in flight per thread
 constexpr int kSlots = kWindow + 1;           // one spare slot between read and refill
 constexpr int kThreads = AR_GENERIC_THREADS;
 constexpr int kStackDepth = 16;               // >= tree height + 1 for P <= AR_MAX_RANKS
-constexpr int kMaxProg = 2 * AR_MAX_RANKS;    // ops of one tree program (2P - 1)
 
 struct GenericParams {
   const uint4* send[AR_MAX_RANKS];
   uint4* recv[AR_MAX_RANKS];
-  const int16_t* prog;  // device: tree 0 program then tree 1 program (prog_len ops each)
-  int prog_len;
+  const int16_t* push;  // device: tree 0's then tree 1's ranks in preorder (P each)
   int P;
   int Q;                // hierarchical: ranks per group (P = G * Q)
   uint64_t count;       // elements per rank (hierarchical sub-chunk lengths)
@@ -196,23 +194,15 @@ __global__ void __launch_bounds__(kThreads) generic_allreduce_kernel(const __gri
   __shared__ uint4 slots[kSlots][kThreads];
   __shared__ const uint4* s_send[AR_MAX_RANKS];
   __shared__ uint4* s_recv[AR_MAX_RANKS];
-  __shared__ int16_t s_prog[2][kMaxProg];   // tree programs
   __shared__ int16_t s_push[2][AR_MAX_RANKS];   // tree leaf (push) sequences
   const int P = p.P;
   const int tid = threadIdx.x;
   for (int r = tid; r < P; r += kThreads) {
     s_send[r] = p.send[r];
     s_recv[r] = p.recv[r];
-  }
-  if constexpr (ALGO == kTree) {
-    for (int t = 0; t < 2; ++t) {
-      for (int i = tid; i < p.prog_len; i += kThreads) s_prog[t][i] = p.prog[t * p.prog_len + i];
-    }
-    __syncthreads();
-    if (tid < 2) {  // leaf order = the program's pushes in order
-      int j = 0;
-      for (int i = 0; i < p.prog_len; ++i)
-        if (s_prog[tid][i] >= 0) s_push[tid][j++] = s_prog[tid][i];
+    if constexpr (ALGO == kTree) {
+      s_push[0][r] = p.push[r];
+      s_push[1][r] = p.push[P + r];
     }
   }
   __syncthreads();
@@ -295,8 +285,7 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
     p.send[r] = static_cast<const uint4*>(c.send[r]);
     p.recv[r] = static_cast<uint4*>(c.recv[r]);
   }
-  p.prog = c.tree_prog;
-  p.prog_len = c.prog_len;
+  p.push = c.tree_push;
   p.P = c.P;
   p.Q = c.group;
   p.count = c.count;
@@ -309,7 +298,7 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
                             : tree_split_vectors(c.count, DT);
   p.scale = c.scale;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
-  if (ALGO == kTree && c.prog_len > kMaxProg) return cudaErrorInvalidValue;
+  if (ALGO == kTree && c.tree_push == nullptr) return cudaErrorInvalidValue;
   const uint64_t columns = p.nfull + (p.tail ? 1 : 0);
   uint64_t grid = (columns + kThreads - 1) / kThreads;
   if (c.max_blocks > 0 && grid > (uint64_t)c.max_blocks) grid = (uint64_t)c.max_blocks;
@@ -348,8 +337,7 @@ cudaError_t launch_scatter_one(const Call& c, LaunchInfo* info) {
     p.send[r] = static_cast<const uint4*>(c.send[r]);
     p.recv[r] = static_cast<uint4*>(c.recv[r]);
   }
-  p.prog = nullptr;
-  p.prog_len = 0;
+  p.push = nullptr;
   p.P = c.P;
   p.Q = c.P;
   p.count = c.count;

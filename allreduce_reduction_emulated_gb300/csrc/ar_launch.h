@@ -22,10 +22,9 @@ struct Call {
   float scale;
   cudaStream_t stream;
   int sms;                  // multiprocessors of the device
-  // TREE for P > kMaxStaticRanks: postorder programs of tree 0 and tree 1
-  // (device memory, 2 * prog_len entries; >= 0 push that rank, -1 combine).
-  const int16_t* tree_prog;
-  int prog_len;
+  // TREE for P > kMaxStaticRanks: tree 0's then tree 1's ranks in the order
+  // their folds consume them (preorder; device memory, P entries each)
+  const int16_t* tree_push;
   // LL protocol state
   unsigned long long* staging;  // P slots of stage_stride 8-byte words
   size_t stage_stride;

@@ -111,8 +111,7 @@ extern "C" ar_status_t ar_allreduce_ll_noalloc(int nranks, const void* const* se
     c.scale = scale;
     c.stream = st;
     c.sms = s.sms;
-    c.tree_prog = nullptr;
-    c.prog_len = 0;
+    c.tree_push = nullptr;
     c.staging = s.base + kSlotsOffset;
     c.stage_stride = kStride;
     c.status = reinterpret_cast<int*>(s.base);
