@@ -425,6 +425,13 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
     e = ar::launch_ll128(call, &info);
   } else if (chosen == AR_ALGO_HIER) {
     e = ar::launch_generic(call, &info);
+  } else if (P <= ar::kMaxStaticRanks && c->max_blocks > 0 && c->max_blocks < c->sms &&
+             count * esize / ar::kTmaTileBytes >= (size_t)c->max_blocks) {
+    // capped to fewer SMs than the GPU has, with at least a tile per block:
+    // the TMA pipeline keeps far more bytes in flight per SM
+    e = dtype == AR_FLOAT32    ? ar::launch_tma_f32(call, &info)
+        : dtype == AR_BFLOAT16 ? ar::launch_tma_bf16(call, &info)
+                               : ar::launch_tma_i32(call, &info);
   } else if (P <= ar::kMaxStaticRanks) {
     e = dtype == AR_FLOAT32    ? ar::launch_static_f32(call, &info)
         : dtype == AR_BFLOAT16 ? ar::launch_static_bf16(call, &info)

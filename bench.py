@@ -51,6 +51,7 @@ PROFILES = {
     "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll128.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32": ("static_reduce_scatter_p8_8MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p8_64MiB_fp32_ring_ddp_mean_64sm": ("tma_ring_p8_64MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_f32.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
 
@@ -87,6 +88,11 @@ WORKLOADS = {
                                    op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter"),
     "p8_ag_8MiB_shards_fp32": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                    op="sum", algo="ring", scale=1.0, seed=0, coll="all_gather"),
+    # the headline on 64 of the 152 SMs (AR_OPT_MAX_BLOCKS): the TMA bulk-copy pipeline, for
+    # an all-reduce that shares the GPU with computation
+    "p8_64MiB_fp32_ring_ddp_mean_64sm": dict(P=8, count=16 * 1024 * 1024, kind="normal", sigma=1e-3,
+                                             dtype="f32", op="sum", algo="ring", scale=0.125, seed=0,
+                                             max_blocks=64),
     # reduce-scatter above the rank-specialised limit: 72 shards of 256 KiB (18 MiB per rank)
     "p72_rs_256KiB_shards_fp32": dict(P=72, count=64 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                       op="sum", algo="ring", scale=1.0 / 72, seed=0, coll="reduce_scatter"),
@@ -115,7 +121,8 @@ DDP_BUCKET = 25 * 1024 * 1024 // 4
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 6000; 200 with --ddp-buckets, 30 with --ddp-overlap)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="p8_64MiB_fp32_ring_ddp_mean")
@@ -144,7 +151,8 @@ def config_of(name: str, w: dict, n: int) -> dict:
             "values": f"{w['kind']} sigma={w['sigma']} seed={w['seed']}",
             "l2": "inputs larger than L2 (no flush)" if 2 * w["P"] * w["count"] * ESIZE[w["dtype"]] > 2 * 129e6
                   else "L2 not flushed (small message: latency-bound)",
-            "parallelism": f"replicas x{n}"}
+            "parallelism": f"replicas x{n}",
+            **({"max_blocks": w["max_blocks"]} if "max_blocks" in w else {})}
 
 
 # ------------------------------------------------------------------ clocks
@@ -398,6 +406,8 @@ def ours_arm(args, w, name):
     comm = ar.ar_init(P)
     if "group" in w:
         ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, w["group"])
+    if "max_blocks" in w:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, w["max_blocks"])
     stream = torch.cuda.current_stream()
 
     def call(xs, ys, s):
@@ -850,6 +860,8 @@ def ddp_overlap(args):
 
 def main():
     args = parse_args()
+    if args.steps is None:
+        args.steps = 30 if args.ddp_overlap else 200 if args.ddp_buckets else 6000
     if args.ddp_overlap:
         ddp_overlap(args)
         return

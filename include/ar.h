@@ -83,7 +83,7 @@ typedef enum {
     AR_ERR_CUDA = 2,         /* a CUDA runtime call failed (no device, launch failure)   */
     AR_ERR_UNSUPPORTED = 3,  /* valid but not provided: scale != 1 for int32 / min / max,
                                 LL above the LL limit                                    */
-    AR_ERR_TIMEOUT = 4,      /* device side: an LL flag wait hit its spin limit         */
+    AR_ERR_TIMEOUT = 4,      /* device side: a flag or mbarrier wait hit its limit      */
     AR_ERR_OOM = 5           /* ar_init could not allocate its device memory            */
 } ar_status_t;
 
@@ -136,7 +136,7 @@ ar_status_t ar_init(int nranks, ar_comm_t* out);
  * Asynchronous: returns after enqueueing one kernel on `stream` (none when
  * count == 0).  Argument errors return synchronously (AR_ERR_INVALID_ARG,
  * AR_ERR_UNSUPPORTED) before anything is enqueued; launch failures return
- * AR_ERR_CUDA; device-side errors (LL spin limit) are reported later by
+ * AR_ERR_CUDA; device-side errors (a wait limit) are reported later by
  * ar_get_status.
  * CUDA graphs: every algorithm may be captured and replayed (the buffers
  * are then fixed).  The LL / LL128 epoch lives in device memory and each
@@ -151,7 +151,8 @@ ar_status_t ar_allreduce(ar_comm_t comm, const void* const* sendbufs, void* cons
 
 /*
  * Device-side status of the calls made so far on `comm`: AR_SUCCESS or
- * AR_ERR_TIMEOUT (an LL flag wait gave up; that call's output is incomplete).
+ * AR_ERR_TIMEOUT (an LL / LL128 flag wait or a TMA-kernel mbarrier wait gave
+ * up; that call's output is incomplete).
  * Reads and clears the device status word with a synchronous copy, so call it
  * after synchronizing the streams the calls ran on.  AR_ERR_CUDA if the copy
  * fails, AR_ERR_INVALID_ARG for a NULL comm.
@@ -178,10 +179,13 @@ ar_status_t ar_select_algo(ar_comm_t comm, size_t count, ar_dtype_t dtype, ar_al
 typedef enum {
     AR_OPT_LL_MAX_BYTES = 0,     /* LL limit in bytes per rank, 16 .. the size given
                                     at ar_init (default 65536 or AR_LL_MAX_BYTES)       */
-    AR_OPT_LL_SPIN_LIMIT = 1,    /* polls of one flag before AR_ERR_TIMEOUT (>= 1)     */
+    AR_OPT_LL_SPIN_LIMIT = 1,    /* polls of one LL / LL128 flag, or of one mbarrier
+                                    phase in the TMA kernel, before AR_ERR_TIMEOUT
+                                    (>= 1)                                          */
     AR_OPT_DEBUG = 2,            /* nonzero: one line per call on stderr               */
-    AR_OPT_LL_SKIP_PRODUCER = 3, /* test hook: LL kernels skip staging, so every flag
-                                    wait runs out and reports AR_ERR_TIMEOUT           */
+    AR_OPT_LL_SKIP_PRODUCER = 3, /* test hook: the LL / LL128 kernels skip staging and
+                                    the TMA kernel's producer issues no copies, so
+                                    every wait runs out and reports AR_ERR_TIMEOUT   */
     AR_OPT_HIER_GROUP = 4,       /* AR_ALGO_HIER ranks per group: a divisor of P
                                     (default 8; a call whose P it does not divide
                                     returns AR_ERR_UNSUPPORTED)                       */
@@ -194,7 +198,10 @@ typedef enum {
                                     all-gather kernels launch at most this many
                                     thread blocks (grid-stride), leaving the other
                                     SMs to kernels on other streams; 0 = no cap
-                                    (default).  Results do not change.              */
+                                    (default).  Below the SM count, ring / tree
+                                    calls with P <= 8 and at least 4 KiB per rank
+                                    per block run the TMA bulk-copy pipeline, one
+                                    block per SM.  Results do not change.           */
     AR_OPT_LL_EPOCH = 8          /* test hook: sets the last epoch used by LL and
                                     LL128 (0 .. 2^32 - 2; the next call uses
                                     value + 1; the call that uses 2^32 - 1 clears

@@ -1,0 +1,120 @@
+"""The TMA bulk-copy all-reduce (P <= 8 capped to fewer SMs than the GPU has)
+against the oracle, bit for bit.
+
+"NCCL, NIXL, and Distributed GPU Communication" (the overlap checklist): the
+all-reduce runs beside computation, so AR_OPT_MAX_BLOCKS gives it a few SMs;
+below the SM count the rank-specialised ring / tree fold runs as a pipeline of
+bulk copies through shared memory.  Same orders as the uncapped kernel, so the
+two agree element for element; ragged counts exercise partial tiles and the
+trailing partial vector; the bounded mbarrier waits are made to run out with
+the producer-skip test hook.
+"""
+import numpy as np
+import pytest
+import torch
+
+import allreduce_reduction_emulated_gb300 as ar
+import oracle
+import pins
+from gpu_util import VEC, Guarded, device_inputs, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+OPS = (ar.AR_SUM, ar.AR_MIN, ar.AR_MAX)
+BLOCKS = 16
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def tma_counts(dtype):
+    V, tile = VEC[dtype], 4096 // (2 if dtype == ar.AR_BFLOAT16 else 4)
+    return [BLOCKS * tile, BLOCKS * tile + 3 * V + 1, 37 * tile + V - 1, 200_003]
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
+def test_capped_calls_match_the_oracle(P, dtype, dev, capfd):
+    rng = np.random.default_rng(800 + 10 * P + dtype)
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        ar.ar_set_option(comm, ar.AR_OPT_DEBUG, 1)
+        for count in tma_counts(dtype):
+            sends = pins.random_inputs(rng, P, count, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            for op in OPS:
+                for algo, oalgo in ((ar.AR_ALGO_RING, oracle.RING), (ar.AR_ALGO_TREE, oracle.TREE)):
+                    scale = 0.125 if (op == ar.AR_SUM and dtype != ar.AR_INT32) else 1.0
+                    outs = [Guarded(count, dtype, dev) for _ in range(P)]
+                    ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, dtype, op, algo, scale)
+                    torch.cuda.synchronize()
+                    assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                    want = oracle.allreduce(sends, dtype, op, oalgo, scale)
+                    for r in range(P):
+                        assert outs[r].guards_intact()
+                        pins.assert_bitwise(to_host(outs[r].tensor), want[r],
+                                            f"P={P} dtype={dtype} count={count} op={op} algo={algo} rank={r}")
+        log = capfd.readouterr().err
+        assert "kernel=tma_ring" in log and "kernel=tma_tree" in log
+    finally:
+        ar.ar_destroy(comm)
+
+
+def test_full_size_equals_the_uncapped_kernel(dev):
+    """8 x 64 MiB fp32, ring, scale 1/8 on 64 SMs: element for element the
+    uncapped kernel's result, in place and out of place."""
+    P, count = 8, 16 * 1024 * 1024
+    comm = ar.ar_init(P)
+    try:
+        sends = device_inputs("normal", 0, P, count, dev, 1e-3)
+        ref = [torch.empty_like(s) for s in sends]
+        got = [torch.empty_like(s) for s in sends]
+        ar.ar_allreduce(comm, sends, ref, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125)
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 64)
+        ar.ar_allreduce(comm, sends, got, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125)
+        torch.cuda.synchronize()
+        for r in range(P):
+            assert torch.equal(got[r].view(torch.int32), ref[r].view(torch.int32)), f"rank {r}"
+        inplace = [s.clone() for s in sends]
+        ar.ar_allreduce(comm, inplace, inplace, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        for r in range(P):
+            assert torch.equal(inplace[r].view(torch.int32), ref[r].view(torch.int32)), f"in place, rank {r}"
+    finally:
+        ar.ar_destroy(comm)
+
+
+def test_bounded_waits_report_a_timeout_and_recover(dev):
+    P, count = 8, 1 << 20
+    comm = ar.ar_init(P)
+    try:
+        rng = np.random.default_rng(12)
+        sends = pins.random_inputs(rng, P, count, ar.AR_FLOAT32)
+        xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+        ys = [torch.zeros_like(x) for x in xs]
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 32)
+        # no tile is ever loaded: every consumer wait, then the producer's, runs out
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SPIN_LIMIT, 2000)
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SKIP_PRODUCER, 1)
+        ar.ar_allreduce(comm, xs, ys, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 1.0)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_ERR_TIMEOUT
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SKIP_PRODUCER, 0)
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SPIN_LIMIT, 1 << 22)
+        ar.ar_allreduce(comm, xs, ys, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 1.0)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        want = oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.RING)
+        pins.assert_bitwise(to_host(ys[6]), want[6], "TMA call after a timed-out one")
+    finally:
+        ar.ar_destroy(comm)
