@@ -17,7 +17,7 @@ from __future__ import annotations
 
 import torch
 
-from . import AR_ALGO_RING, AR_SUM, ar_allreduce, dtype_of
+from . import AR_ALGO_RING, AR_OPT_MAX_BLOCKS, AR_SUM, ar_allreduce, ar_set_option, dtype_of
 
 
 class BucketReducer:
@@ -27,10 +27,13 @@ class BucketReducer:
     bucket    elements per bucket (the last one may be shorter)
     comm      an ar_init communicator for P ranks
     out       optional P result tensors (default: reduce in place)
+    max_blocks    if given, AR_OPT_MAX_BLOCKS is set to it on the communicator
+                  before each bucket's all-reduce: the all-reduces then run on a
+                  few SMs (the TMA pipeline) beside the backward pass
     """
 
     def __init__(self, comm: int, grads, bucket: int, scale: float = 1.0, algo: int = AR_ALGO_RING,
-                 out=None, stream: torch.cuda.Stream | None = None):
+                 out=None, stream: torch.cuda.Stream | None = None, max_blocks: int | None = None):
         self.comm = comm
         self.grads = list(grads)
         self.out = list(out) if out is not None else self.grads
@@ -42,6 +45,7 @@ class BucketReducer:
         self.stream = stream if stream is not None else torch.cuda.Stream()
         self.starts = list(range(0, self.total, bucket))
         self.next_bucket = 0
+        self.max_blocks = max_blocks
 
     def reset(self):
         self.next_bucket = 0
@@ -57,6 +61,8 @@ class BucketReducer:
                 break
             if n == 0:
                 self.stream.wait_event(event)
+            if self.max_blocks is not None:
+                ar_set_option(self.comm, AR_OPT_MAX_BLOCKS, self.max_blocks)
             ar_allreduce(self.comm, [g[s:e] for g in self.grads], [o[s:e] for o in self.out], e - s,
                          self.dtype, AR_SUM, self.algo, self.scale, self.stream)
             self.next_bucket += 1

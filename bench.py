@@ -790,11 +790,10 @@ def ddp_overlap(args):
     gen = torch.Generator(device=dev).manual_seed(11)
     acts = {d: [torch.randn(T, d, device=dev, generator=gen) * 0.01 for _ in range(P)] for d in (2048, 6144, 8192)}
     comm = ar.ar_init(P)
-    if args.comm_blocks:
-        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, args.comm_blocks)
     compute = torch.cuda.Stream()
     high = torch.cuda.Stream.priority_range()[1] if args.comm_priority else 0
-    reducer = BucketReducer(comm, grads, B, scale=0.125, out=outs, stream=torch.cuda.Stream(priority=high))
+    reducer = BucketReducer(comm, grads, B, scale=0.125, out=outs, stream=torch.cuda.Stream(priority=high),
+                            max_blocks=args.comm_blocks)
     torch.cuda.synchronize()                    # inputs made on the default stream
 
     def backward(overlap):
