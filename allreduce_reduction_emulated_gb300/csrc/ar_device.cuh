@@ -153,13 +153,19 @@ __device__ __forceinline__ uint4 narrow(Acc<DT> a, float scale, bool do_scale) {
 // stored element by element, the missing lanes read as zero and not stored.
 template <int DT>
 __device__ __forceinline__ uint4 load_partial(const uint4* p, int n) {
+  // unrolled over the vector's lanes with a predicate per lane, so the
+  // words stay in registers
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if constexpr (Lanes<DT>::kBytes == 4) {
     const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
-    for (int i = 0; i < n; ++i) w[i] = q[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i < n) w[i] = q[i];
   } else {
     const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
-    for (int i = 0; i < n; ++i) w[i >> 1] |= (uint32_t)q[i] << (16 * (i & 1));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < n) w[i >> 1] |= (uint32_t)q[i] << (16 * (i & 1));
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -169,10 +175,14 @@ __device__ __forceinline__ void store_partial(uint4* p, uint4 v, int n) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   if constexpr (Lanes<DT>::kBytes == 4) {
     uint32_t* q = reinterpret_cast<uint32_t*>(p);
-    for (int i = 0; i < n; ++i) q[i] = w[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i < n) q[i] = w[i];
   } else {
     uint16_t* q = reinterpret_cast<uint16_t*>(p);
-    for (int i = 0; i < n; ++i) q[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < n) q[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
   }
 }
 

@@ -27,10 +27,6 @@ namespace ar {
 
 namespace {
 
-#ifndef AR_LL_COOPERATIVE
-#define AR_LL_COOPERATIVE 1   // 0 only for latency experiments: co-residency is then not guaranteed
-#endif
-
 constexpr int kLLThreads = 256;
 constexpr int kLLBatch = 8;  // staged words polled together (loads in flight)
 
@@ -202,13 +198,8 @@ cudaError_t launch_ll_one(const Call& c, LaunchInfo* info) {
   p.bpr = (int)bpr;
   const int grid = c.P * p.bpr;
   void* args[] = {&p};
-#if AR_LL_COOPERATIVE
   cudaError_t e = cudaLaunchCooperativeKernel((const void*)kernel, dim3(grid), dim3(kLLThreads), args,
                                               0, c.stream);
-#else
-  kernel<<<grid, kLLThreads, 0, c.stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-#endif
   info->kernel = "ll";
   info->grid = grid;
   info->block = kLLThreads;
