@@ -327,6 +327,45 @@ def pin_tree_structure(O):
             assert interiors[0] | interiors[1] == set(range(P)), f"P={P}: {interiors}"
 
 
+def tree_from_definition(P: int, t: int) -> str:
+    """The double binary tree written out from its definition ("NCCL and
+    NVSHMEM -- two GPU communication models, side by side", the double binary
+    tree paragraph, read as R2 / R4): labels 1..P in an in-order tree rooted at
+    the largest power of two <= P; a label v with b = v & -v >= 2 has the left
+    child v - b/2 and the right child v + h, h the largest of b/2, b/4, ... with
+    v + h <= P; tree 0 gives label v to rank v - 1, tree 1 to rank v mod P; a
+    node's value is ((own + left) + right)."""
+    def rank(v):
+        return v - 1 if t == 0 else v % P
+
+    def node(v):
+        b = v & -v
+        expr = f"x{rank(v)}"
+        if b >= 2:
+            expr = f"({expr}+{node(v - b // 2)})"
+            h = b // 2
+            while h >= 1 and v + h > P:
+                h //= 2
+            if h >= 1:
+                expr = f"({expr}+{node(v + h)})"
+        return expr
+
+    root = 1
+    while root * 2 <= P:
+        root *= 2
+    return node(root)
+
+
+def pin_tree_definition(O):
+    """Every rank count the library takes (1..256): the oracle's two trees are
+    the definition's, written out independently here."""
+    for P in range(1, 257):
+        for t in (0, 1):
+            want = tree_from_definition(P, t)
+            got = O.tree_expr(P, t)
+            assert got == want, f"P={P} tree {t}: {got[:80]} != {want[:80]}"
+
+
 def pin_signed_zero_ties(O):
     """Min / max keep the earlier operand of a +0 / -0 tie, in fold order.
 
@@ -683,7 +722,7 @@ def pin_hierarchical_order_independent(O):
 
 
 ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_tree_expressions,
-            pin_tree_structure, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
+            pin_tree_structure, pin_tree_definition, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
             pin_sampled_matches_full, pin_reduce_scatter_worked_example, pin_all_gather_worked_example,
             pin_allreduce_is_reduce_scatter_then_all_gather, pin_reduce_scatter_ring_steps,
             pin_collectives_order_independent, pin_hierarchical_steps,
