@@ -30,7 +30,9 @@ def dev():
     return torch.device("cuda:0")
 
 
-def test_overlapped_buckets_match_serial_and_oracle(dev):
+@pytest.mark.parametrize("max_blocks", [None, 16])
+def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks):
+    """max_blocks=16: the bucket all-reduces run on 16 SMs (the TMA pipeline)."""
     P, T, bucket = 4, 96, 300_000
     shapes = [(512, 1024), (1024, 512), (512, 768)] * 2          # 6 "parameters", backward order
     total = sum(m * n for m, n in shapes)
@@ -43,7 +45,7 @@ def test_overlapped_buckets_match_serial_and_oracle(dev):
             grads = [torch.zeros(total, device=dev) for _ in range(P)]
             outs = [torch.full((total,), float("nan"), device=dev) for _ in range(P)]
             compute = torch.cuda.Stream()
-            red = BucketReducer(comm, grads, bucket, scale=0.25, out=outs)
+            red = BucketReducer(comm, grads, bucket, scale=0.25, out=outs, max_blocks=max_blocks)
             torch.cuda.synchronize()              # buffers initialised on the default stream
             with torch.cuda.stream(compute):
                 off = 0
