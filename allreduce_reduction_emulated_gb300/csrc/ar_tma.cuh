@@ -34,6 +34,8 @@
 // spans warps after the start, so a warp that stops cannot block another.
 #pragma once
 
+#include <atomic>
+
 #include "../../include/ar.h"
 #include "ar_static.cuh"
 
@@ -251,9 +253,17 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   p.status = c.status;
   p.spin_limit = c.spin_limit;
   p.skip_produce = c.skip_produce;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NP>());
-  if (attr != cudaSuccess) return attr;
+  // the shared-memory opt-in is a per-device attribute: set it once on each device
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NP>());
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
   uint64_t grid = (uint64_t)(c.max_blocks > 0 ? c.max_blocks : c.sms);
   if (grid > (uint64_t)c.sms) grid = (uint64_t)c.sms;  // one block per SM
   if (grid > p.ntiles) grid = p.ntiles;
