@@ -226,7 +226,7 @@ const char* ar_get_error_string(ar_status_t s) {
     case AR_ERR_INVALID_ARG: return "invalid argument";
     case AR_ERR_CUDA: return "CUDA runtime error";
     case AR_ERR_UNSUPPORTED: return "unsupported argument combination";
-    case AR_ERR_TIMEOUT: return "LL flag wait timed out";
+    case AR_ERR_TIMEOUT: return "device-side wait timed out (LL flag or TMA barrier)";
     case AR_ERR_OOM: return "out of device memory";
     default: return "unknown status";
   }
