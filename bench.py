@@ -47,6 +47,8 @@ PROFILES = {
     "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll.cu"], 1.0),
     "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_4MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_16MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p72_16MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll128.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32": ("static_reduce_scatter_p8_8MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
@@ -77,6 +79,8 @@ WORKLOADS = {
                                     dtype="i32", op="sum", algo="ring", scale=1.0, seed=0),
     "p72_4MiB_int32_max_tree": dict(P=72, count=1024 * 1024, kind="int", sigma=1.0,
                                     dtype="i32", op="max", algo="tree", scale=1.0, seed=0),
+    "p72_4MiB_int32_sum_hier": dict(P=72, count=1024 * 1024, kind="int", sigma=1.0,
+                                    dtype="i32", op="sum", algo="hier", scale=1.0, seed=0, group=8),
     "p72_4MiB_fp32_sum_hier": dict(P=72, count=1024 * 1024, kind="normal", sigma=1e-3,
                                    dtype="f32", op="sum", algo="hier", scale=1.0 / 72, seed=3, group=8),
     "p8_512KiB_fp32_ll128": dict(P=8, count=128 * 1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
