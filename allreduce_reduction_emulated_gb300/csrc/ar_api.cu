@@ -475,6 +475,12 @@ ar_status_t ar_reduce_scatter(ar_comm_t c, const void* const* sendbufs, void* co
   cudaError_t e;
   if (!vec) {
     e = ar::launch_reduce_scatter_elem(call, &info);
+  } else if (c->P <= ar::kMaxStaticRanks && c->max_blocks > 0 && c->max_blocks < c->sms &&
+             call.count * ar::elem_bytes(dtype) / ar::kTmaTileBytes >= (size_t)c->max_blocks) {
+    // capped to fewer SMs than the GPU has: the TMA pipeline, shard-owner stores
+    e = dtype == AR_FLOAT32    ? ar::launch_tma_f32(call, &info)
+        : dtype == AR_BFLOAT16 ? ar::launch_tma_bf16(call, &info)
+                               : ar::launch_tma_i32(call, &info);
   } else if (c->P <= ar::kMaxStaticRanks) {  // rank-specialised, shard-owner stores
     e = dtype == AR_FLOAT32    ? ar::launch_static_f32(call, &info)
         : dtype == AR_BFLOAT16 ? ar::launch_static_bf16(call, &info)

@@ -59,8 +59,9 @@ inline size_t elem_bytes(int dtype) { return dtype == 1 ? 2 : 4; }
 cudaError_t launch_static_f32(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
-// the same all-reduce (P <= kMaxStaticRanks, ring or tree) as a TMA bulk-copy
-// pipeline, one block per SM on c.max_blocks SMs: for calls that share the GPU
+// the same all-reduce (P <= kMaxStaticRanks, ring or tree; or the ring
+// reduce-scatter when c.shard != 0) as a TMA bulk-copy pipeline, one block per
+// SM on c.max_blocks SMs: for calls that share the GPU
 cudaError_t launch_tma_f32(const Call& c, LaunchInfo* info);
 cudaError_t launch_tma_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_tma_i32(const Call& c, LaunchInfo* info);

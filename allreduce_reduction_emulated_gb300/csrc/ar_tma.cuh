@@ -27,6 +27,9 @@
 //                          stage's previous tile belonged to the same warp
 //                          (CW divides the stage count), so that lane's own
 //                          bulk-group wait guards the output tile's reuse.
+// The reduce-scatter variant (SCATTER, ring only) is the same pipeline: shard
+// s is ring chunk s, and the output tile goes to its shard's owner only (a
+// tile that straddles a shard boundary is stored segment by segment).
 // Every mbarrier wait is bounded: on its limit the thread records
 // AR_ERR_TIMEOUT and stops; the producer then waits (bounded) for the loads
 // it issued and each storing lane for its bulk stores, so no copy is in
@@ -43,14 +46,21 @@ namespace ar {
 
 namespace tma {
 
-constexpr int kTile = (int)kTmaTileBytes;  // bytes per rank per stage
-constexpr int kStages = 6;
-constexpr int kConsumerWarps = 2;           // divides kStages
-constexpr int kThreads = 32 + 32 * kConsumerWarps;
-static_assert(kStages % kConsumerWarps == 0, "a stage's tiles must stay with one warp");
+// Pipeline shape per mode (measured, 8 ranks fp32 on 32 / 48 / 64 SMs):
+// the all-reduce moves P tiles in and P out per tile and runs best with
+// 4 KiB tiles in 6 stages; the reduce-scatter (P in, 1 out) with 8 KiB tiles
+// in 3 stages.  2 KiB tiles halve either rate, whatever the stage count.
+template <bool SCATTER>
+struct Shape {
+  static constexpr int kTile = SCATTER ? 2 * (int)kTmaTileBytes : (int)kTmaTileBytes;  // bytes per rank
+  static constexpr int kStages = SCATTER ? 3 : 6;
+  static constexpr int kConsumerWarps = 3;  // divides kStages
+  static constexpr int kThreads = 32 + 32 * kConsumerWarps;
+  static_assert(kStages % kConsumerWarps == 0, "a stage's tiles must stay with one warp");
+};
 
-template <int NP>
-constexpr size_t smem_bytes() { return (size_t)kStages * (NP + 1) * kTile; }
+template <int NP, bool SCATTER>
+constexpr size_t smem_bytes() { return (size_t)Shape<SCATTER>::kStages * (NP + 1) * Shape<SCATTER>::kTile; }
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -99,7 +109,7 @@ struct Params {
   const char* send[NP];
   char* recv[NP];
   uint64_t bytes;   // whole 16-byte vectors per rank, in bytes
-  uint64_t ntiles;  // ceil(bytes / kTile)
+  uint64_t ntiles;  // ceil(bytes / tile)
   uint64_t split;   // ring: vectors per chunk; tree: first vector of tree 1
   float scale;
   int do_scale;
@@ -125,8 +135,11 @@ __device__ __forceinline__ uint4 fold_column(const uint4 (&r)[NP], int order, ui
   }
 }
 
-template <int NP, int DT, int OP, int ALGO>
-__global__ void __launch_bounds__(kThreads, 1) allreduce_kernel(const __grid_constant__ Params<NP> p) {
+template <int NP, int DT, int OP, int ALGO, bool SCATTER = false>
+__global__ void __launch_bounds__(Shape<SCATTER>::kThreads, 1) allreduce_kernel(const __grid_constant__ Params<NP> p) {
+  constexpr int kTile = Shape<SCATTER>::kTile;
+  constexpr int kStages = Shape<SCATTER>::kStages;
+  constexpr int kConsumerWarps = Shape<SCATTER>::kConsumerWarps;
   extern __shared__ __align__(128) char smem[];
   char* const in = smem;                                  // [stage][slot][kTile]
   char* const out = smem + (size_t)kStages * NP * kTile;  // [stage][kTile]
@@ -215,15 +228,29 @@ __global__ void __launch_bounds__(kThreads, 1) allreduce_kernel(const __grid_con
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&empty[s]);  // the input slots are free
+      if constexpr (SCATTER) {
+        const uint64_t sb = p.split * 16;  // shard bytes
+        if (ord != kPerElement) {
+          bulk_store(p.recv[ord] + (off - (uint64_t)ord * sb), tout, len);
+        } else {  // the tile crosses shard boundaries: one store per shard segment
+          for (uint64_t pos = off; pos < off + len;) {
+            const uint64_t c = pos / sb;
+            const uint64_t end = (c + 1) * sb < off + len ? (c + 1) * sb : off + len;
+            bulk_store(p.recv[c] + (pos - c * sb), tout + (pos - off), (uint32_t)(end - pos));
+            pos = end;
+          }
+        }
+      } else {
 #pragma unroll
-      for (int k = 0; k < NP; ++k) bulk_store(p.recv[k] + off, tout, len);
+        for (int k = 0; k < NP; ++k) bulk_store(p.recv[k] + off, tout, len);
+      }
       bulk_commit();
     }
   }
   if (lane == 0) {
     bulk_wait_all();
     // the trailing partial vector, element by element in the same order
-    if (p.tail != 0 && blockIdx.x == 0 && w == 0) {
+    if (!SCATTER && p.tail != 0 && blockIdx.x == 0 && w == 0) {
       const uint64_t n = p.bytes / 16;
       uint4 r[NP];
 #pragma unroll
@@ -235,9 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) allreduce_kernel(const __grid_con
   }
 }
 
-template <int DT, int NP, int OP, int ALGO>
+template <int DT, int NP, int OP, int ALGO, bool SCATTER = false>
 cudaError_t launch_one(const Call& c, LaunchInfo* info) {
-  auto kernel = allreduce_kernel<NP, DT, OP, ALGO>;
+  auto kernel = allreduce_kernel<NP, DT, OP, ALGO, SCATTER>;
+  constexpr int kTile = Shape<SCATTER>::kTile;
+  constexpr size_t kSmem = smem_bytes<NP, SCATTER>();
   Params<NP> p;
   for (int k = 0; k < NP; ++k) {
     p.send[k] = static_cast<const char*>(c.send[k]);
@@ -248,6 +277,11 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   p.ntiles = (p.bytes + kTile - 1) / kTile;
   p.tail = (int)(c.count % V);
   p.split = ALGO == kRing ? ring_chunk_vectors(c.count, NP, DT) : tree_split_vectors(c.count, DT);
+  if constexpr (SCATTER) {  // shards of whole vectors: shard s is chunk s
+    if (c.shard % V != 0 || c.count != (size_t)NP * c.shard) return cudaErrorInvalidValue;
+    p.split = c.shard / V;
+    p.tail = 0;
+  }
   p.scale = c.scale;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   p.status = c.status;
@@ -260,7 +294,7 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
   if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NP>());
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -268,16 +302,24 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   if (grid > (uint64_t)c.sms) grid = (uint64_t)c.sms;  // one block per SM
   if (grid > p.ntiles) grid = p.ntiles;
   if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, kThreads, smem_bytes<NP>(), c.stream>>>(p);
-  info->kernel = ALGO == kRing ? "tma_ring" : "tma_tree";
+  kernel<<<(unsigned)grid, Shape<SCATTER>::kThreads, kSmem, c.stream>>>(p);
+  info->kernel = SCATTER ? "tma_reduce_scatter" : ALGO == kRing ? "tma_ring" : "tma_tree";
   info->grid = (int)grid;
-  info->block = kThreads;
-  info->smem = smem_bytes<NP>();
+  info->block = Shape<SCATTER>::kThreads;
+  info->smem = kSmem;
   return cudaGetLastError();
 }
 
 template <int DT, int NP>
 cudaError_t launch_np(const Call& c, LaunchInfo* info) {
+  if (c.shard != 0) {  // reduce-scatter
+    switch (c.op) {
+      case kSum: return launch_one<DT, NP, kSum, kRing, true>(c, info);
+      case kMin: return launch_one<DT, NP, kMin, kRing, true>(c, info);
+      case kMax: return launch_one<DT, NP, kMax, kRing, true>(c, info);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (c.op * 4 + c.algo) {
     case kSum * 4 + kRing: return launch_one<DT, NP, kSum, kRing>(c, info);
     case kSum * 4 + kTree: return launch_one<DT, NP, kSum, kTree>(c, info);

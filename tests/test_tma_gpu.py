@@ -1,5 +1,5 @@
-"""The TMA bulk-copy all-reduce (P <= 8 capped to fewer SMs than the GPU has)
-against the oracle, bit for bit.
+"""The TMA bulk-copy all-reduce and reduce-scatter (P <= 8 capped to fewer SMs
+than the GPU has) against the oracle, bit for bit.
 
 "NCCL, NIXL, and Distributed GPU Communication" (the overlap checklist): the
 all-reduce runs beside computation, so AR_OPT_MAX_BLOCKS gives it a few SMs;
@@ -116,5 +116,56 @@ def test_bounded_waits_report_a_timeout_and_recover(dev):
         assert ar.ar_get_status(comm) == ar.AR_SUCCESS
         want = oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.RING)
         pins.assert_bitwise(to_host(ys[6]), want[6], "TMA call after a timed-out one")
+    finally:
+        ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 8])
+@pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
+def test_capped_reduce_scatter_matches_the_oracle(P, dtype, dev, capfd):
+    """Reduce-scatter on 16 SMs: shard s folded in ring chunk s's order, stored
+    to its owner only; shards of whole 4 KiB tiles and shards whose edges fall
+    inside a tile (stored segment by segment)."""
+    rng = np.random.default_rng(900 + 10 * P + dtype)
+    comm = ar.ar_init(P)
+    used = False
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        ar.ar_set_option(comm, ar.AR_OPT_DEBUG, 1)
+        for rc in (16384, 20000, 50000):
+            sends = pins.random_inputs(rng, P, P * rc, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            for op in OPS:
+                scale = 0.125 if (op == ar.AR_SUM and dtype != ar.AR_INT32) else 1.0
+                outs = [Guarded(rc, dtype, dev) for _ in range(P)]
+                ar.ar_reduce_scatter(comm, xs, [o.tensor for o in outs], rc, dtype, op, scale)
+                torch.cuda.synchronize()
+                assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                want = oracle.reduce_scatter(sends, dtype, op, scale)
+                for r in range(P):
+                    assert outs[r].guards_intact()
+                    pins.assert_bitwise(to_host(outs[r].tensor), want[r],
+                                        f"RS P={P} dtype={dtype} rc={rc} op={op} rank={r}")
+        used = "kernel=tma_reduce_scatter" in capfd.readouterr().err
+    finally:
+        ar.ar_destroy(comm)
+    assert used
+
+
+def test_capped_reduce_scatter_in_place(dev):
+    P, rc = 8, 20000
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        rng = np.random.default_rng(31)
+        sends = pins.random_inputs(rng, P, P * rc, ar.AR_FLOAT32)
+        want = oracle.reduce_scatter(sends, ar.AR_FLOAT32, ar.AR_SUM, 0.125)
+        big = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+        ar.ar_reduce_scatter(comm, big, [big[r][r * rc:(r + 1) * rc] for r in range(P)], rc,
+                             ar.AR_FLOAT32, ar.AR_SUM, 0.125)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        for r in range(P):
+            pins.assert_bitwise(to_host(big[r][r * rc:(r + 1) * rc]), want[r], f"in place rank {r}")
     finally:
         ar.ar_destroy(comm)
