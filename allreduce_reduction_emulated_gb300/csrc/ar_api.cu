@@ -8,6 +8,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/ar.h"
 #include "ar_device.cuh"
 #include "ar_launch.h"
@@ -74,6 +76,36 @@ void emit_preorder(int v, int P, int t, std::vector<int16_t>& out) {
   const int l = ar::tree_left(v), r = ar::tree_right(v, P);
   if (l) emit_preorder(l, P, t, out);
   if (r) emit_preorder(r, P, t, out);
+}
+
+// One NVTX range per collective call, around its launch, in a domain of its
+// own (so a caller's default-domain ranges and filters are unaffected).
+// Header-only NVTX: a no-op unless a profiler is attached.
+nvtxDomainHandle_t nvtx_domain() {
+  static const nvtxDomainHandle_t d = nvtxDomainCreateA("allreduce_emulated");
+  return d;
+}
+
+struct Range {
+  explicit Range(const char* name) {
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(nvtx_domain(), &a);
+  }
+  ~Range() { nvtxDomainRangePop(nvtx_domain()); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
+const char* allreduce_range(ar_algo_t a) {
+  return a == AR_ALGO_RING   ? "ar_allreduce ring"
+         : a == AR_ALGO_TREE ? "ar_allreduce tree"
+         : a == AR_ALGO_LL   ? "ar_allreduce ll"
+         : a == AR_ALGO_LL128 ? "ar_allreduce ll128"
+                             : "ar_allreduce hier";
 }
 
 const char* dtype_name(int d) { return d == AR_FLOAT32 ? "f32" : d == AR_BFLOAT16 ? "bf16" : "i32"; }
@@ -411,6 +443,7 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
   call.stage_words = 0;
   call.shard = 0;
 
+  Range range(allreduce_range(chosen));
   ar::LaunchInfo info;
   cudaError_t e;
   if (chosen == AR_ALGO_LL) {
@@ -471,6 +504,7 @@ ar_status_t ar_reduce_scatter(ar_comm_t c, const void* const* sendbufs, void* co
   call.dtype = dtype;
   call.op = op;
   call.scale = scale;
+  Range range("ar_reduce_scatter");
   ar::LaunchInfo info;
   cudaError_t e;
   if (!vec) {
@@ -512,6 +546,7 @@ ar_status_t ar_all_gather(ar_comm_t c, const void* const* sendbufs, void* const*
   call.shard = sendcount;
   call.dtype = dtype;
   call.algo = vec ? 1 : 0;  // 1: 16-byte vector copy
+  Range range("ar_all_gather");
   ar::LaunchInfo info;
   cudaError_t e = ar::launch_all_gather(call, &info);
   if (c->debug)
