@@ -548,7 +548,14 @@ ar_status_t ar_all_gather(ar_comm_t c, const void* const* sendbufs, void* const*
   call.algo = vec ? 1 : 0;  // 1: 16-byte vector copy
   Range range("ar_all_gather");
   ar::LaunchInfo info;
-  cudaError_t e = ar::launch_all_gather(call, &info);
+  cudaError_t e;
+  if (vec && c->max_blocks > 0 && c->max_blocks < c->sms &&
+      call.count * ar::elem_bytes(dtype) / ar::kTmaGatherTileBytes >= (size_t)c->max_blocks) {
+    // capped to fewer SMs than the GPU has, with at least a tile per block
+    e = ar::launch_all_gather_tma(call, &info);
+  } else {
+    e = ar::launch_all_gather(call, &info);
+  }
   if (c->debug)
     std::fprintf(stderr, "[ar] all_gather P=%d sendcount=%zu dtype=%s kernel=%s grid=%d status=%s\n",
                  c->P, sendcount, dtype_name(dtype), info.kernel, info.grid, cudaGetErrorString(e));

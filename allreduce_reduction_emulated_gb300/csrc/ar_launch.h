@@ -67,6 +67,9 @@ cudaError_t launch_tma_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_tma_i32(const Call& c, LaunchInfo* info);
 // bytes per rank per pipeline tile of the TMA kernel
 constexpr size_t kTmaTileBytes = 4096;
+// the all-gather (any P) as a TMA pipeline on c.max_blocks SMs; its tile size
+cudaError_t launch_all_gather_tma(const Call& c, LaunchInfo* info);
+constexpr size_t kTmaGatherTileBytes = 32768;
 cudaError_t launch_generic(const Call& c, LaunchInfo* info);
 cudaError_t launch_ll(const Call& c, LaunchInfo* info);
 // LL128: 128-byte lines of 120 payload bytes + a flag word (staging, stage_stride)

@@ -55,6 +55,7 @@ PROFILES = {
     "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p8_64MiB_fp32_ring_ddp_mean_64sm": ("tma_ring_p8_64MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_f32.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32_64sm": ("tma_reduce_scatter_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_f32.cu"], 1.0),
+    "p8_ag_8MiB_shards_fp32_64sm": ("tma_all_gather_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_gather.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
 
@@ -101,6 +102,10 @@ WORKLOADS = {
     # the reduce-scatter on 64 SMs (TMA pipeline): gradient shards beside computation
     "p8_rs_8MiB_shards_fp32_64sm": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                         op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter",
+                                        max_blocks=64),
+    # the all-gather on 64 SMs (TMA pipeline)
+    "p8_ag_8MiB_shards_fp32_64sm": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
+                                        op="sum", algo="ring", scale=1.0, seed=0, coll="all_gather",
                                         max_blocks=64),
     # reduce-scatter above the rank-specialised limit: 72 shards of 256 KiB (18 MiB per rank)
     "p72_rs_256KiB_shards_fp32": dict(P=72, count=64 * 1024, kind="normal", sigma=1e-3, dtype="f32",

@@ -199,9 +199,12 @@ typedef enum {
                                     thread blocks (grid-stride), leaving the other
                                     SMs to kernels on other streams; 0 = no cap
                                     (default).  Below the SM count, ring / tree
-                                    calls with P <= 8 and at least 4 KiB per rank
-                                    per block run the TMA bulk-copy pipeline, one
-                                    block per SM.  Results do not change.           */
+                                    all-reduces and reduce-scatters with P <= 8
+                                    and at least 4 KiB per rank per block, and
+                                    all-gathers of whole 16-byte pieces with at
+                                    least 32 KiB per block, run TMA bulk-copy
+                                    pipelines, one block per SM.  Results do not
+                                    change.                                         */
     AR_OPT_LL_EPOCH = 8          /* test hook: sets the last epoch used by LL and
                                     LL128 (0 .. 2^32 - 2; the next call uses
                                     value + 1; the call that uses 2^32 - 1 clears

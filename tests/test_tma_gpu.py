@@ -1,5 +1,5 @@
-"""The TMA bulk-copy all-reduce and reduce-scatter (P <= 8 capped to fewer SMs
-than the GPU has) against the oracle, bit for bit.
+"""The TMA bulk-copy all-reduce, reduce-scatter (P <= 8) and all-gather (any
+P), capped to fewer SMs than the GPU has, against the oracle, bit for bit.
 
 "NCCL, NIXL, and Distributed GPU Communication" (the overlap checklist): the
 all-reduce runs beside computation, so AR_OPT_MAX_BLOCKS gives it a few SMs;
@@ -167,5 +167,71 @@ def test_capped_reduce_scatter_in_place(dev):
         assert ar.ar_get_status(comm) == ar.AR_SUCCESS
         for r in range(P):
             pins.assert_bitwise(to_host(big[r][r * rc:(r + 1) * rc]), want[r], f"in place rank {r}")
+    finally:
+        ar.ar_destroy(comm)
+
+
+def ag_counts(P, dtype):
+    """Shard lengths giving at least BLOCKS tiles of 32 KiB in all: whole tiles
+    and a ragged last tile (still whole 16-byte vectors)."""
+    es, V = (2, 8) if dtype == ar.AR_BFLOAT16 else (4, 4)
+    base = -(-BLOCKS * 32768 // (P * es) // V) * V
+    return [base, base + 3 * V, 4 * base + V]
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 8, 13, 72])
+@pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
+def test_capped_all_gather_matches_the_oracle(P, dtype, dev, capfd):
+    rng = np.random.default_rng(950 + 10 * P + dtype)
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        ar.ar_set_option(comm, ar.AR_OPT_DEBUG, 1)
+        for sc in ag_counts(P, dtype):
+            pieces = pins.random_inputs(rng, P, sc, dtype)
+            xs = [to_device(a, dtype, dev) for a in pieces]
+            outs = [Guarded(P * sc, dtype, dev) for _ in range(P)]
+            ar.ar_all_gather(comm, xs, [o.tensor for o in outs], sc, dtype)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            want = oracle.all_gather(pieces, dtype)
+            for r in (0, P // 2, P - 1):
+                assert outs[r].guards_intact()
+                pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"AG P={P} dtype={dtype} sc={sc} rank={r}")
+        assert "kernel=tma_all_gather" in capfd.readouterr().err
+    finally:
+        ar.ar_destroy(comm)
+
+
+def test_capped_all_gather_in_place_and_timeout(dev):
+    P, sc = 8, 100_004
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        rng = np.random.default_rng(41)
+        pieces = pins.random_inputs(rng, P, sc, ar.AR_FLOAT32)
+        full = [torch.zeros(P * sc, device=dev) for _ in range(P)]
+        for r in range(P):
+            full[r][r * sc:(r + 1) * sc] = torch.from_numpy(pieces[r]).to(dev)
+        ar.ar_all_gather(comm, [full[r][r * sc:(r + 1) * sc] for r in range(P)], full, sc, ar.AR_FLOAT32)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        want = oracle.all_gather(pieces, ar.AR_FLOAT32)
+        for r in range(P):
+            pins.assert_bitwise(to_host(full[r]), want[r], f"in place rank {r}")
+        # no tile is ever loaded: the bounded waits run out and report
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SPIN_LIMIT, 2000)
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SKIP_PRODUCER, 1)
+        outs = [torch.zeros(P * sc, device=dev) for _ in range(P)]
+        srcs = [to_device(a, ar.AR_FLOAT32, dev) for a in pieces]
+        ar.ar_all_gather(comm, srcs, outs, sc, ar.AR_FLOAT32)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_ERR_TIMEOUT
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SKIP_PRODUCER, 0)
+        ar.ar_set_option(comm, ar.AR_OPT_LL_SPIN_LIMIT, 1 << 22)
+        ar.ar_all_gather(comm, srcs, outs, sc, ar.AR_FLOAT32)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        pins.assert_bitwise(to_host(outs[5]), want[5], "after a timed-out call")
     finally:
         ar.ar_destroy(comm)
