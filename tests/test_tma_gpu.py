@@ -235,3 +235,43 @@ def test_capped_all_gather_in_place_and_timeout(dev):
         pins.assert_bitwise(to_host(outs[5]), want[5], "after a timed-out call")
     finally:
         ar.ar_destroy(comm)
+
+
+FIRST_CALL_CAPTURED = r"""
+import sys
+import numpy as np, torch
+sys.path.insert(0, {root!r})
+import allreduce_reduction_emulated_gb300 as ar
+torch.cuda.set_device(0)
+dev = torch.device("cuda:0")
+P, n = 8, 1 << 20
+xs = [torch.full((n,), float(r + 1), device=dev) for r in range(P)]
+ys = [torch.zeros(n, device=dev) for _ in range(P)]
+comm = ar.ar_init(P)
+ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 16)
+torch.cuda.synchronize()
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.stream(s):
+    with torch.cuda.graph(g, stream=s):          # the process's first capped call
+        ar.ar_allreduce(comm, xs, ys, n, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125, s)
+g.replay()
+torch.cuda.synchronize()
+assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+assert bool((ys[3] == 4.5).all())                # (1 + ... + 8) / 8
+ar.ar_destroy(comm)
+print("ok")
+"""
+
+
+def test_first_capped_call_inside_a_graph_capture(dev):
+    """The kernel's shared-memory opt-in happens on a device's first capped
+    call; here that call is being captured (in a fresh process)."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", FIRST_CALL_CAPTURED.format(root=root)],
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
