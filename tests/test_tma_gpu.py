@@ -275,3 +275,37 @@ def test_first_capped_call_inside_a_graph_capture(dev):
     out = subprocess.run([sys.executable, "-c", FIRST_CALL_CAPTURED.format(root=root)],
                          capture_output=True, text=True, timeout=300)
     assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
+
+
+def test_full_size_reduce_scatter_and_all_gather_on_64_sms(dev):
+    """P=8, 8 MiB shards / pieces (the bench's sizes): the capped TMA kernels
+    equal the uncapped kernels element for element, and sampled reduce-scatter
+    outputs equal the oracle."""
+    P, rc = 8, 2 * 1024 * 1024
+    comm = ar.ar_init(P)
+    try:
+        sends = device_inputs("normal", 0, P, P * rc, dev, 1e-3)
+        ref = [torch.empty(rc, device=dev) for _ in range(P)]
+        got = [torch.empty(rc, device=dev) for _ in range(P)]
+        ar.ar_reduce_scatter(comm, sends, ref, rc, ar.AR_FLOAT32, ar.AR_SUM, 0.125)
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 64)
+        ar.ar_reduce_scatter(comm, sends, got, rc, ar.AR_FLOAT32, ar.AR_SUM, 0.125)
+        gathered = [torch.empty(P * rc, device=dev) for _ in range(P)]
+        ar.ar_all_gather(comm, got, gathered, rc, ar.AR_FLOAT32)
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 0)
+        gathered_ref = [torch.empty(P * rc, device=dev) for _ in range(P)]
+        ar.ar_all_gather(comm, ref, gathered_ref, rc, ar.AR_FLOAT32)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        for r in range(P):
+            assert torch.equal(got[r].view(torch.int32), ref[r].view(torch.int32)), f"RS rank {r}"
+            assert torch.equal(gathered[r].view(torch.int32), gathered_ref[r].view(torch.int32)), f"AG rank {r}"
+        rng = np.random.default_rng(6)
+        idx = np.unique(np.concatenate([rng.integers(0, P * rc, 512), [0, rc - 1, rc, P * rc - 1]]))
+        it = torch.from_numpy(idx).to(dev)
+        cols = np.stack([to_host(s.index_select(0, it)) for s in sends])
+        want = oracle.allreduce_sampled(cols, idx, P * rc, ar.AR_FLOAT32, oracle.SUM, oracle.RING, 0.125)
+        flat = torch.cat(got)
+        pins.assert_bitwise(to_host(flat.index_select(0, it)), want, "sampled capped reduce-scatter outputs")
+    finally:
+        ar.ar_destroy(comm)
