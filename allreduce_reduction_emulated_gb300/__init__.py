@@ -90,8 +90,29 @@ def library() -> ctypes.CDLL:
     return _lib
 
 
-def _ptr(x) -> int:
-    return x if isinstance(x, int) else x.data_ptr()
+_ESIZE = {AR_FLOAT32: 4, AR_BFLOAT16: 2, AR_INT32: 4}
+
+
+def _ptr(x, elems: int, dtype: int, what: str) -> int:
+    """Device address of a buffer: a raw pointer (int) is passed through; a
+    tensor must be contiguous CUDA memory of at least `elems` elements of the
+    data type's size, else ArError(AR_ERR_INVALID_ARG) -- the library only sees
+    a pointer, so these are the checks it cannot make."""
+    if isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ArError(AR_ERR_INVALID_ARG, f"{what}: tensor is not contiguous")
+    if not x.is_cuda:
+        raise ArError(AR_ERR_INVALID_ARG, f"{what}: tensor is not in CUDA memory")
+    if x.element_size() != _ESIZE.get(int(dtype), 0):
+        raise ArError(AR_ERR_INVALID_ARG, f"{what}: {x.element_size()}-byte elements for this data type")
+    if x.numel() < elems:
+        raise ArError(AR_ERR_INVALID_ARG, f"{what}: {x.numel()} elements, {elems} needed")
+    return x.data_ptr()
+
+
+def _ptrs(bufs, elems: int, dtype: int, what: str):
+    return (ctypes.c_void_p * len(bufs))(*[_ptr(b, elems, dtype, f"{what}[{i}]") for i, b in enumerate(bufs)])
 
 
 def _stream_handle(stream) -> int:
@@ -129,8 +150,8 @@ def ar_allreduce(comm: int, sendbufs, recvbufs, count: int, dtype: int, op: int 
     P = len(sendbufs)
     if len(recvbufs) != P:
         raise ArError(AR_ERR_INVALID_ARG, "ar_allreduce: sendbufs and recvbufs differ in length")
-    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
-    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    sp = _ptrs(sendbufs, int(count), dtype, "ar_allreduce sendbufs")
+    rp = _ptrs(recvbufs, int(count), dtype, "ar_allreduce recvbufs")
     st = library().ar_allreduce(comm, sp, rp, int(count), int(dtype), int(op), int(algo),
                                 float(scale), _stream_handle(stream))
     if st != AR_SUCCESS:
@@ -143,8 +164,8 @@ def ar_reduce_scatter(comm: int, sendbufs, recvbufs, recvcount: int, dtype: int,
     P = len(sendbufs)
     if len(recvbufs) != P:
         raise ArError(AR_ERR_INVALID_ARG, "ar_reduce_scatter: sendbufs and recvbufs differ in length")
-    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
-    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    sp = _ptrs(sendbufs, P * int(recvcount), dtype, "ar_reduce_scatter sendbufs")
+    rp = _ptrs(recvbufs, int(recvcount), dtype, "ar_reduce_scatter recvbufs")
     st = library().ar_reduce_scatter(comm, sp, rp, int(recvcount), int(dtype), int(op), float(scale),
                                      _stream_handle(stream))
     if st != AR_SUCCESS:
@@ -156,8 +177,8 @@ def ar_all_gather(comm: int, sendbufs, recvbufs, sendcount: int, dtype: int, str
     P = len(sendbufs)
     if len(recvbufs) != P:
         raise ArError(AR_ERR_INVALID_ARG, "ar_all_gather: sendbufs and recvbufs differ in length")
-    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
-    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    sp = _ptrs(sendbufs, int(sendcount), dtype, "ar_all_gather sendbufs")
+    rp = _ptrs(recvbufs, P * int(sendcount), dtype, "ar_all_gather recvbufs")
     st = library().ar_all_gather(comm, sp, rp, int(sendcount), int(dtype), _stream_handle(stream))
     if st != AR_SUCCESS:
         raise ArError(st, "ar_all_gather")
@@ -203,8 +224,8 @@ def ar_allreduce_ll_noalloc(sendbufs, recvbufs, count: int, dtype: int, op: int 
     P = len(sendbufs)
     if len(recvbufs) != P:
         raise ArError(AR_ERR_INVALID_ARG, "ar_allreduce_ll_noalloc: sendbufs and recvbufs differ in length")
-    sp = (ctypes.c_void_p * P)(*[_ptr(b) for b in sendbufs])
-    rp = (ctypes.c_void_p * P)(*[_ptr(b) for b in recvbufs])
+    sp = _ptrs(sendbufs, int(count), dtype, "ar_allreduce_ll_noalloc sendbufs")
+    rp = _ptrs(recvbufs, int(count), dtype, "ar_allreduce_ll_noalloc recvbufs")
     status = ctypes.c_int(-1)
     st = library().ar_allreduce_ll_noalloc(P, sp, rp, int(count), int(dtype), int(op), float(scale),
                                            _stream_handle(stream),

@@ -80,3 +80,59 @@ def test_product_path_does_not_touch_the_oracle():
         if path.endswith((".py", ".cu", ".cuh", ".h")):
             text = open(path).read()
             assert "oracle" not in text.lower(), f"{path} mentions the oracle"
+
+
+def test_binding_rejects_tensors_the_library_cannot_check():
+    """The C ABI sees only pointers: the binding refuses tensors that are not
+    contiguous, not in CUDA memory, too short or of the wrong element size
+    before any call reaches the library (so these run without a GPU)."""
+    import torch
+
+    x = torch.zeros(64)
+    cases = [
+        (lambda: ar.ar_allreduce(1, [x[::2]], [x[::2]], 8, ar.AR_FLOAT32), "not contiguous"),
+        (lambda: ar.ar_allreduce(1, [x], [x], 8, ar.AR_FLOAT32), "not in CUDA memory"),
+        (lambda: ar.ar_reduce_scatter(1, [x, x], [x, x], 40, ar.AR_FLOAT32), "not in CUDA memory"),
+        (lambda: ar.ar_all_gather(1, [x], [x[:3].clone()], 8, ar.AR_FLOAT32), "not in CUDA memory"),
+    ]
+    for call, reason in cases:
+        with pytest.raises(ar.ArError) as e:
+            call()
+        assert e.value.status == ar.AR_ERR_INVALID_ARG and reason in str(e.value)
+
+
+def test_binding_checks_length_and_element_size(monkeypatch):
+    """Length and element size, with the CUDA check satisfied by a stand-in."""
+    import torch
+
+    class CudaLike:
+        def __init__(self, t):
+            self.t = t
+            self.is_cuda = True
+
+        def is_contiguous(self):
+            return self.t.is_contiguous()
+
+        def element_size(self):
+            return self.t.element_size()
+
+        def numel(self):
+            return self.t.numel()
+
+        def data_ptr(self):
+            return self.t.data_ptr()
+
+    short = CudaLike(torch.zeros(7))
+    wide = CudaLike(torch.zeros(16, dtype=torch.float64))
+    with pytest.raises(ar.ArError) as e:
+        ar._ptrs([short], 8, ar.AR_FLOAT32, "x")
+    assert "7 elements, 8 needed" in str(e.value)
+    with pytest.raises(ar.ArError) as e:
+        ar._ptrs([wide], 8, ar.AR_FLOAT32, "x")
+    assert "8-byte elements" in str(e.value)
+    ok = CudaLike(torch.zeros(8, dtype=torch.int16))
+    assert ar._ptrs([ok], 8, ar.AR_BFLOAT16, "x")[0] == ok.data_ptr()
+    # reduce-scatter inputs need P * recvcount elements, all-gather outputs too
+    with pytest.raises(ar.ArError) as e:
+        ar._ptrs([CudaLike(torch.zeros(15))], 2 * 8, ar.AR_FLOAT32, "x")
+    assert "15 elements, 16 needed" in str(e.value)
