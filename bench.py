@@ -293,6 +293,28 @@ def job_gbs(bytes_per_replica_step: float, ms_per_step: float, world: int) -> fl
 
 # -------------------------------------------------------------- CPU oracle
 
+HOST_CORES = os.cpu_count() or 1
+
+
+class OneCore:
+    """Pins the calling thread to one host core while the (single-threaded)
+    oracle is timed, then restores its affinity."""
+
+    def __enter__(self):
+        self.saved = None
+        if hasattr(os, "sched_getaffinity"):
+            try:
+                self.saved = os.sched_getaffinity(0)
+                os.sched_setaffinity(0, {max(self.saved)})
+            except OSError:
+                self.saved = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+
+
 def oracle_throughput(w: dict, host_sends, seconds: float):
     """The oracle as it stands, one host core, over whole-workload passes."""
     import numpy as np
@@ -309,20 +331,21 @@ def oracle_throughput(w: dict, host_sends, seconds: float):
     if coll == "allreduce" and algo is not None:
         recvs = [np.zeros(count, dtype=oracle.NP_DTYPE[dt]) for _ in range(P)]
         oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, min(count, 65536), recvs)  # warm
-    done, t0 = 0, time.perf_counter()
-    while True:
-        if coll == "reduce_scatter":
-            oracle.reduce_scatter(host_sends, dt, op, w["scale"])
-        elif coll == "all_gather":
-            oracle.all_gather(host_sends, dt)
-        elif algo is None:
-            oracle.allreduce_hier(host_sends, w["group"], dt, op, w["scale"])
-        else:
-            oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, count, recvs)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
+    with OneCore():
+        done, t0 = 0, time.perf_counter()
+        while True:
+            if coll == "reduce_scatter":
+                oracle.reduce_scatter(host_sends, dt, op, w["scale"])
+            elif coll == "all_gather":
+                oracle.all_gather(host_sends, dt)
+            elif algo is None:
+                oracle.allreduce_hier(host_sends, w["group"], dt, op, w["scale"])
+            else:
+                oracle.allreduce(host_sends, dt, op, algo, w["scale"], 0, count, recvs)
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
     return done * nccl_bytes / el / 1e9, done, el
 
 
@@ -361,10 +384,11 @@ def reference_arm(args, w, name):
             sends[r][probe:S] = synthetic.values_np(w["kind"], w["seed"], r, idx, w["sigma"])
     for _ in range(args.warmup):
         oracle.allreduce(sends, dt, op, algo, w["scale"], 0, S, recvs)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.allreduce(sends, dt, op, algo, w["scale"], 0, S, recvs)
-    el = time.perf_counter() - t0
+    with OneCore():
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.allreduce(sends, dt, op, algo, w["scale"], 0, S, recvs)
+        el = time.perf_counter() - t0
     value = S * ESIZE[w["dtype"]] * args.steps / el / 1e9
     sample = (f"elements [0, {S}) of each of the {P} ranks' {count}-element buffers per step "
               f"(ring chunking of the full count), one host core")
@@ -374,7 +398,8 @@ def reference_arm(args, w, name):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
         "data": "synthetic", "config": config_of(name, w, args.gpus),
         "busbw": value * 2 * (P - 1) / P,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": HOST_CORES, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -528,7 +553,7 @@ def ours_arm(args, w, name):
             host_np = [h.numpy() if h.dtype != torch.bfloat16 else h.view(torch.int16).numpy().view(np.uint16)
                        for h in host_in]
             gbs, passes, el = oracle_throughput(w, host_np, args.cpu_seconds)
-            cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            cpu = {"value": gbs, "unit": UNIT, "cores": 1, "host_cores": HOST_CORES, "kind": "oracle",
                    "sample": f"{passes} full pass(es) over the workload ({P} x {n_in} input elements), "
                              f"{el:.1f} s on one host core"}
         traffic = profiled_traffic(name)
@@ -739,9 +764,10 @@ def ddp_buckets(args):
     nb_cpu, done, t_cpu = 0, 0, 0.0
     for start, n in buckets:
         host = [x[start:start + n].cpu().numpy() for x in sends]
-        c0 = time.perf_counter()
-        oracle.allreduce(host, oracle.F32, oracle.SUM, oracle.RING, 0.125)
-        t_cpu += time.perf_counter() - c0
+        with OneCore():
+            c0 = time.perf_counter()
+            oracle.allreduce(host, oracle.F32, oracle.SUM, oracle.RING, 0.125)
+            t_cpu += time.perf_counter() - c0
         nb_cpu += 1
         done += n
         if t_cpu >= args.cpu_seconds:
@@ -760,7 +786,8 @@ def ddp_buckets(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_kind} HBM copy bandwidth"},
-        "cpu_baseline": {"value": done * 4 / t_cpu / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": done * 4 / t_cpu / 1e9, "unit": UNIT, "cores": 1, "host_cores": HOST_CORES,
+                         "kind": "oracle",
                          "sample": f"the first {nb_cpu} bucket all-reduces ({done} elements per rank)"},
         "e2e": None, "gpu_launches": len(buckets) * args.steps,
         "clocks": clocks.summary(t0, t1),

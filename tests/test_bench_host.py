@@ -84,3 +84,14 @@ def test_traffic_only_while_the_sources_match(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda s: "0" * 16)
     assert bench.profiled_traffic(name) is None
     assert bench.profiled_traffic("no_such_workload") is None
+
+
+def test_oracle_timing_runs_on_one_core():
+    import os
+
+    if not hasattr(os, "sched_getaffinity"):
+        pytest.skip("no affinity control on this platform")
+    before = os.sched_getaffinity(0)
+    with bench.OneCore():
+        assert len(os.sched_getaffinity(0)) == 1
+    assert os.sched_getaffinity(0) == before
