@@ -65,7 +65,8 @@ cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
 cudaError_t launch_tma_f32(const Call& c, LaunchInfo* info);
 cudaError_t launch_tma_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_tma_i32(const Call& c, LaunchInfo* info);
-// bytes per rank per pipeline tile of the TMA kernel
+// the TMA kernel is chosen when every block gets at least this many bytes per
+// rank (its tiles are 6 or 8 KiB; a block with fewer bytes has little to pipeline)
 constexpr size_t kTmaTileBytes = 4096;
 // the all-gather (any P) as a TMA pipeline on c.max_blocks SMs; its tile size
 cudaError_t launch_all_gather_tma(const Call& c, LaunchInfo* info);

@@ -46,15 +46,15 @@ namespace ar {
 
 namespace tma {
 
-// Pipeline shape per mode (measured, 8 ranks fp32 on 32 / 48 / 64 SMs):
-// the all-reduce moves P tiles in and P out per tile and runs best with
-// 4 KiB tiles in 6 stages; the reduce-scatter (P in, 1 out) with 8 KiB tiles
-// in 3 stages.  2 KiB tiles halve either rate, whatever the stage count.
+// Pipeline shape per mode (measured, 8 ranks fp32 on 48 / 64 SMs): the
+// all-reduce (P tiles in, P out) runs best with 6 KiB tiles in 4 stages and 2
+// consumer warps; the reduce-scatter (P in, 1 out) with 8 KiB tiles in 3
+// stages and 3 warps.  2 KiB tiles halve either rate, whatever the stage count.
 template <bool SCATTER>
 struct Shape {
-  static constexpr int kTile = SCATTER ? 2 * (int)kTmaTileBytes : (int)kTmaTileBytes;  // bytes per rank
-  static constexpr int kStages = SCATTER ? 3 : 6;
-  static constexpr int kConsumerWarps = 3;  // divides kStages
+  static constexpr int kTile = SCATTER ? 8192 : 6144;  // bytes per rank; multiples of 16
+  static constexpr int kStages = SCATTER ? 3 : 4;
+  static constexpr int kConsumerWarps = SCATTER ? 3 : 2;  // divides kStages
   static constexpr int kThreads = 32 + 32 * kConsumerWarps;
   static_assert(kStages % kConsumerWarps == 0, "a stage's tiles must stay with one warp");
 };
