@@ -95,3 +95,22 @@ def test_oracle_timing_runs_on_one_core():
     with bench.OneCore():
         assert len(os.sched_getaffinity(0)) == 1
     assert os.sched_getaffinity(0) == before
+
+
+def test_clock_summary_reads_nvidia_smi_rows():
+    """The clocks record of a bench line: the median SM clock inside the timed
+    region, the maximum, and every throttle reason seen Active there."""
+    c = bench.ClockSampler(0)
+    row = lambda sm, hw="Not Active", thermal="Not Active", cap="Not Active": \
+        [f.strip() for f in f"0, {sm}, 2070, 900.1, 0x0, {hw}, {thermal}, Not Active, {cap}".split(",")]
+    c.rows = [(0.5, row(1200)), (1.0, row(2070)), (1.5, row(2070, cap="Active")), (2.0, row(1965)),
+              (2.5, row(2070)), (9.0, row(300, thermal="Active"))]
+    s = c.summary(1.0, 2.5)
+    assert s["samples_in_timed_region"] == 4 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]              # the thermal sample lies outside the region
+    s = c.summary(8.5, 9.5)
+    assert s["reasons"] == ["hw_thermal_slowdown"] and s["sm_mhz"] == 300.0
+    # no sample inside the region: fall back to every sample; malformed rows are skipped
+    c.rows.append((3.0, ["0", "[N/A]"]))
+    s = c.summary(100.0, 101.0)
+    assert s["samples_in_timed_region"] == 0 and s["samples"] == 7 and s["sm_mhz"] == 2070.0
