@@ -150,3 +150,30 @@ def test_epoch_option_arguments(dev):
         ar.ar_set_option(comm, ar.AR_OPT_LL_EPOCH, 0xFFFFFFFE)
     finally:
         ar.ar_destroy(comm)
+
+
+def test_many_back_to_back_calls(dev):
+    """20,000 LL / LL128 calls in a row on one stream, sizes changing: each
+    call's last block publishes the epoch the next call starts from.  Checked
+    against the ring every few hundred calls and for the device status."""
+    P = 8
+    comm = ar.ar_init(P)
+    try:
+        rng = np.random.default_rng(2024)
+        top = 16384
+        sends = pins.random_inputs(rng, P, top, ar.AR_FLOAT32)
+        xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+        ys = [torch.empty_like(x) for x in xs]
+        ref = [torch.empty_like(x) for x in xs]
+        counts = rng.integers(1, top + 1, size=20000)
+        for i, n in enumerate(counts):
+            algo = ar.AR_ALGO_LL if i % 2 == 0 else ar.AR_ALGO_LL128
+            ar.ar_allreduce(comm, xs, ys, int(n), ar.AR_FLOAT32, ar.AR_SUM, algo, 1.0)
+            if i % 997 == 0:
+                ar.ar_allreduce(comm, xs, ref, int(n), ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 1.0)
+                torch.cuda.synchronize()
+                assert torch.equal(ys[i % P][:n].view(torch.int32), ref[i % P][:n].view(torch.int32)), f"call {i}"
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+    finally:
+        ar.ar_destroy(comm)
