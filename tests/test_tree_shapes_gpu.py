@@ -1,5 +1,5 @@
-"""Tree and ring order above eight ranks, over the tree shapes the rank count
-produces ("NCCL and NVSHMEM -- two GPU communication models, side by side",
+"""Tree and ring order (and the LL protocols) above eight ranks, over the tree
+shapes the rank count produces ("NCCL and NVSHMEM -- two GPU communication models, side by side",
 the double binary tree).
 
 The kernel for P > 8 walks the in-order lowbit tree's right spine and folds
@@ -53,5 +53,28 @@ def test_tree_and_ring_orders_for_many_ranks(P, dev):
                     assert outs[r].guards_intact()
                     pins.assert_bitwise(to_host(outs[r].tensor), want[r],
                                         f"P={P} dtype={dtype} op={op} count={count} algo={algo} rank={r}")
+    finally:
+        ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P", [17, 129, 256])
+def test_ll_protocols_at_many_ranks(P, dev):
+    """LL and LL128 with up to AR_MAX_RANKS ranks (the widest parameter block;
+    every rank's block group resident at once), against the oracle's ring."""
+    rng = np.random.default_rng(700 + P)
+    comm = ar.ar_init(P)
+    try:
+        for algo in (ar.AR_ALGO_LL, ar.AR_ALGO_LL128):
+            for count in (5, 1001, 16384):
+                sends = pins.random_inputs(rng, P, count, ar.AR_FLOAT32)
+                xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+                outs = [Guarded(count, ar.AR_FLOAT32, dev) for _ in range(P)]
+                ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, ar.AR_FLOAT32, ar.AR_SUM, algo, 1.0)
+                torch.cuda.synchronize()
+                assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                want = oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.RING, 1.0)
+                for r in (0, P - 1):
+                    assert outs[r].guards_intact()
+                    pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"P={P} algo={algo} count={count} rank={r}")
     finally:
         ar.ar_destroy(comm)
