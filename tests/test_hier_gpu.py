@@ -28,7 +28,7 @@ def dev():
 
 
 @pytest.mark.parametrize("P,Q", [(2, 1), (4, 2), (6, 3), (8, 4), (8, 8), (9, 3), (12, 4), (16, 8),
-                                 (72, 8), (72, 9), (72, 1)])
+                                 (72, 8), (72, 9), (72, 1), (128, 8), (256, 16), (256, 256)])
 def test_hier_small(P, Q, dev):
     rng = np.random.default_rng(900 + P * 7 + Q)
     comm = ar.ar_init(P)
