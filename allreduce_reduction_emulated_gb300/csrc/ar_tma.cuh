@@ -2,7 +2,7 @@
 // bulk-copy pipeline, for calls limited to a few SMs (AR_OPT_MAX_BLOCKS).
 //
 // The load/store-unit kernel needs most of the GPU to reach full HBM
-// bandwidth: a block keeps about 64 KiB in flight, ~45 GB/s.  When the
+// bandwidth: a block keeps about 64 KiB in flight, ~70 GB/s at most.  When the
 // all-reduce shares the GPU with computation (the DDP overlap of "NCCL,
 // NIXL, and Distributed GPU Communication", its overlap checklist), it gets
 // a few dozen SMs, so each SM must keep far more bytes in flight.  One block
@@ -16,7 +16,7 @@
 //                          tile offset advances (no division per tile, which
 //                          would slow the single issuing thread).  The
 //                          stage's order (rotation / tree, or "per element"
-//                          for the one tile that straddles a boundary) goes
+//                          for a tile that straddles a boundary) goes
 //                          to order[s], published by the barrier arrival;
 //   consumer warps         warp w takes whole tiles w, w + CW, ...: waits on
 //                          full[s], folds each 16-byte column of the NP
