@@ -46,21 +46,24 @@ namespace ar {
 
 namespace tma {
 
-// Pipeline shape per mode (measured, 8 ranks fp32 on 48 / 64 SMs): the
-// all-reduce (P tiles in, P out) runs best with 6 KiB tiles in 4 stages and 2
-// consumer warps; the reduce-scatter (P in, 1 out) with 8 KiB tiles in 3
-// stages and 3 warps.  2 KiB tiles halve either rate, whatever the stage count.
-template <bool SCATTER>
+// Pipeline shape per mode (measured, 8 ranks on 48 / 64 SMs): the all-reduce
+// (P tiles in, P out) runs best with 6 KiB tiles in 4 stages and 2 consumer
+// warps for fp32 / int32, 4 for bf16, whose fold widens and re-packs 8 lanes
+// per column; the reduce-scatter (P in, 1 out) with 8 KiB tiles in 3 stages
+// and 3 warps.  2 KiB tiles halve either rate, whatever the stage count.
+template <bool SCATTER, int DT>
 struct Shape {
   static constexpr int kTile = SCATTER ? 8192 : 6144;  // bytes per rank; multiples of 16
   static constexpr int kStages = SCATTER ? 3 : 4;
-  static constexpr int kConsumerWarps = SCATTER ? 3 : 2;  // divides kStages
+  static constexpr int kConsumerWarps = SCATTER ? 3 : DT == kBF16 ? 4 : 2;  // divides kStages
   static constexpr int kThreads = 32 + 32 * kConsumerWarps;
   static_assert(kStages % kConsumerWarps == 0, "a stage's tiles must stay with one warp");
 };
 
-template <int NP, bool SCATTER>
-constexpr size_t smem_bytes() { return (size_t)Shape<SCATTER>::kStages * (NP + 1) * Shape<SCATTER>::kTile; }
+template <int NP, bool SCATTER, int DT>
+constexpr size_t smem_bytes() {
+  return (size_t)Shape<SCATTER, DT>::kStages * (NP + 1) * Shape<SCATTER, DT>::kTile;
+}
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -136,10 +139,10 @@ __device__ __forceinline__ uint4 fold_column(const uint4 (&r)[NP], int order, ui
 }
 
 template <int NP, int DT, int OP, int ALGO, bool SCATTER = false>
-__global__ void __launch_bounds__(Shape<SCATTER>::kThreads, 1) allreduce_kernel(const __grid_constant__ Params<NP> p) {
-  constexpr int kTile = Shape<SCATTER>::kTile;
-  constexpr int kStages = Shape<SCATTER>::kStages;
-  constexpr int kConsumerWarps = Shape<SCATTER>::kConsumerWarps;
+__global__ void __launch_bounds__(Shape<SCATTER, DT>::kThreads, 1) allreduce_kernel(const __grid_constant__ Params<NP> p) {
+  constexpr int kTile = Shape<SCATTER, DT>::kTile;
+  constexpr int kStages = Shape<SCATTER, DT>::kStages;
+  constexpr int kConsumerWarps = Shape<SCATTER, DT>::kConsumerWarps;
   extern __shared__ __align__(128) char smem[];
   char* const in = smem;                                  // [stage][slot][kTile]
   char* const out = smem + (size_t)kStages * NP * kTile;  // [stage][kTile]
@@ -265,8 +268,8 @@ __global__ void __launch_bounds__(Shape<SCATTER>::kThreads, 1) allreduce_kernel(
 template <int DT, int NP, int OP, int ALGO, bool SCATTER = false>
 cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   auto kernel = allreduce_kernel<NP, DT, OP, ALGO, SCATTER>;
-  constexpr int kTile = Shape<SCATTER>::kTile;
-  constexpr size_t kSmem = smem_bytes<NP, SCATTER>();
+  constexpr int kTile = Shape<SCATTER, DT>::kTile;
+  constexpr size_t kSmem = smem_bytes<NP, SCATTER, DT>();
   Params<NP> p;
   for (int k = 0; k < NP; ++k) {
     p.send[k] = static_cast<const char*>(c.send[k]);
@@ -302,10 +305,10 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   if (grid > (uint64_t)c.sms) grid = (uint64_t)c.sms;  // one block per SM
   if (grid > p.ntiles) grid = p.ntiles;
   if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, Shape<SCATTER>::kThreads, kSmem, c.stream>>>(p);
+  kernel<<<(unsigned)grid, Shape<SCATTER, DT>::kThreads, kSmem, c.stream>>>(p);
   info->kernel = SCATTER ? "tma_reduce_scatter" : ALGO == kRing ? "tma_ring" : "tma_tree";
   info->grid = (int)grid;
-  info->block = Shape<SCATTER>::kThreads;
+  info->block = Shape<SCATTER, DT>::kThreads;
   info->smem = kSmem;
   return cudaGetLastError();
 }
