@@ -152,6 +152,8 @@ def parse_args():
     ap.add_argument("--comm-blocks", type=int, default=0,
                     help="--ddp-overlap: cap the all-reduce kernels at this many thread blocks (0 = none); "
                          "below the SM count they run the TMA pipeline, one block per SM (48 measured best)")
+    ap.add_argument("--grad-dtype", choices=("fp32", "bf16"), default="fp32",
+                    help="--ddp-overlap: gradient dtype (bf16: bf16 GEMMs and bf16 bucket all-reduces)")
     ap.add_argument("--comm-priority", action="store_true",
                     help="--ddp-overlap: run the communication stream at the highest priority")
     ap.add_argument("--sweep", action="store_true",
@@ -803,9 +805,10 @@ DDP_LAYER_SHAPES = [(2048, 8192), (8192, 2048), (2048, 6144), (2048, 2048)]
 
 def ddp_overlap(args):
     """The 1.2B-parameter DDP step on 8 emulated ranks: backward = per-rank
-    weight-gradient GEMMs dW = X^T dY (TF32, tokens x shapes below) written
-    straight into each rank's flat gradient buffer in reverse layer order;
-    communication = 185 x 25 MiB bucket all-reduces (ring, scale 1/8).  Four
+    weight-gradient GEMMs dW = X^T dY (TF32 into fp32 gradients, or bf16 with
+    --grad-dtype bf16; tokens x shapes below) written straight into each rank's
+    flat gradient buffer in reverse layer order; communication = 25 MiB bucket
+    all-reduces (ring, scale 1/8; 185 buckets of fp32, 93 of bf16).  Four
     variants, each one CUDA graph: compute only, comm only, compute then comm,
     and overlapped (each bucket's all-reduce enqueued on a second stream as
     soon as its gradients are written)."""
@@ -819,8 +822,10 @@ def ddp_overlap(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     torch.backends.cuda.matmul.allow_tf32 = True
-    P, T, total, B = 8, args.tokens, DDP_PARAMS, DDP_BUCKET
-    grads = [torch.zeros(total, dtype=torch.float32, device=dev) for _ in range(P)]
+    gdt = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
+    esize = 2 if args.grad_dtype == "bf16" else 4
+    P, T, total, B = 8, args.tokens, DDP_PARAMS, 25 * 1024 * 1024 // esize
+    grads = [torch.zeros(total, dtype=gdt, device=dev) for _ in range(P)]
     outs = [torch.empty_like(g) for g in grads]
     order = [(layer, i) for layer in reversed(range(24)) for i in range(4)]
     views, off = [], 0
@@ -830,7 +835,8 @@ def ddp_overlap(args):
         off += m * n
     assert off == total
     gen = torch.Generator(device=dev).manual_seed(11)
-    acts = {d: [torch.randn(T, d, device=dev, generator=gen) * 0.01 for _ in range(P)] for d in (2048, 6144, 8192)}
+    acts = {d: [(torch.randn(T, d, device=dev, generator=gen) * 0.01).to(gdt) for _ in range(P)]
+            for d in (2048, 6144, 8192)}
     comm = ar.ar_init(P)
     compute = torch.cuda.Stream()
     high = torch.cuda.Stream.priority_range()[1] if args.comm_priority else 0
@@ -887,7 +893,9 @@ def ddp_overlap(args):
     flops = P * 2.0 * total * T
     model = max(times["compute"], times["comm"])
     print(json.dumps({
-        "ddp_overlap": "P=8 x 1,207,959,552 fp32 gradients, 185 x 25 MiB buckets, ring, scale 1/8",
+        "ddp_overlap": f"P=8 x 1,207,959,552 {args.grad_dtype} gradients, "
+                       f"{(total + B - 1) // B} x 25 MiB buckets, ring, scale 1/8",
+        "grad_dtype": args.grad_dtype,
         "tokens_per_rank": T, "steps": args.steps, "unit": "ms",
         "comm_blocks": args.comm_blocks, "comm_priority": bool(args.comm_priority),
         "compute_ms": times["compute"], "comm_ms": times["comm"], "serial_ms": times["serial"],
@@ -895,7 +903,7 @@ def ddp_overlap(args):
         "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,
         "hidden_fraction_of_shorter": (times["serial"] - times["overlap"]) / min(times["compute"], times["comm"]),
         "gemm_tflops": flops / (times["compute"] * 1e-3) / 1e12,
-        "comm_hbm_gbs": 2 * P * total * 4 / (times["comm"] * 1e-3) / 1e9,
+        "comm_hbm_gbs": 2 * P * total * esize / (times["comm"] * 1e-3) / 1e9,
     }), flush=True)
 
 
