@@ -30,20 +30,22 @@ def dev():
     return torch.device("cuda:0")
 
 
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 @pytest.mark.parametrize("max_blocks", [None, 16])
-def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks):
-    """max_blocks=16: the bucket all-reduces run on 16 SMs (the TMA pipeline)."""
+def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks, gdt):
+    """max_blocks=16: the bucket all-reduces run on 16 SMs (the TMA pipeline).
+    bf16: bf16 GEMMs write bf16 gradients, reduced with fp32 accumulation."""
     P, T, bucket = 4, 96, 300_000
     shapes = [(512, 1024), (1024, 512), (512, 768)] * 2          # 6 "parameters", backward order
     total = sum(m * n for m, n in shapes)
     gen = torch.Generator(device=dev).manual_seed(3)
-    acts = {d: [torch.randn(T, d, device=dev, generator=gen) for _ in range(P)] for d in (512, 768, 1024)}
+    acts = {d: [torch.randn(T, d, device=dev, generator=gen).to(gdt) for _ in range(P)] for d in (512, 768, 1024)}
     comm = ar.ar_init(P)
     results = {}
     try:
         for overlap in (False, True):
-            grads = [torch.zeros(total, device=dev) for _ in range(P)]
-            outs = [torch.full((total,), float("nan"), device=dev) for _ in range(P)]
+            grads = [torch.zeros(total, dtype=gdt, device=dev) for _ in range(P)]
+            outs = [torch.full((total,), float("nan"), dtype=gdt, device=dev) for _ in range(P)]
             compute = torch.cuda.Stream()
             red = BucketReducer(comm, grads, bucket, scale=0.25, out=outs, max_blocks=max_blocks)
             torch.cuda.synchronize()              # buffers initialised on the default stream
@@ -73,5 +75,6 @@ def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks):
         pins.assert_bitwise(o_over[r], o_serial[r], f"overlapped vs serial rank {r}")
     for s in range(0, total, bucket):
         e = min(s + bucket, total)
-        want = oracle.allreduce([g[s:e] for g in g_over], oracle.F32, oracle.SUM, oracle.RING, 0.25)
+        odt = oracle.BF16 if gdt == torch.bfloat16 else oracle.F32
+        want = oracle.allreduce([g[s:e] for g in g_over], odt, oracle.SUM, oracle.RING, 0.25)
         pins.assert_bitwise(o_over[P - 1][s:e], want[P - 1], f"bucket at {s}")
