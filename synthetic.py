@@ -19,7 +19,8 @@ Distributions (all exact or rounded once, so host and device agree):
   normal(0, sigma) : Irwin-Hall with 12 draws: K = sum_j (u_j >> 8) as an integer,
                      fp32(K - 6 * 2^24) * 2^-24 * fp32(sigma)       (sigma = std dev)
   int uniform      : (u mod (hi - lo + 1)) + lo                      (int32)
-  bf16             : round-to-nearest-even of the fp32 value
+  bf16             : round-to-nearest-even of the fp32 value ('normal_bf16',
+                     'uniform_bf16')
 """
 from __future__ import annotations
 
@@ -79,9 +80,11 @@ def bf16_bits_np(x: np.ndarray) -> np.ndarray:
 
 
 def values_np(kind: str, seed: int, rank: int, idx, sigma: float = 1.0) -> np.ndarray:
-    """kind: 'uniform' (fp32), 'normal' (fp32), 'normal_bf16' (uint16 bits), 'int'."""
+    """kind: 'uniform' / 'normal' (fp32), 'uniform_bf16' / 'normal_bf16' (uint16 bits), 'int'."""
     if kind == "uniform":
         return uniform_np(seed, rank, idx)
+    if kind == "uniform_bf16":
+        return bf16_bits_np(uniform_np(seed, rank, idx))
     if kind == "normal":
         return normal_np(seed, rank, idx, sigma)
     if kind == "normal_bf16":
@@ -116,9 +119,10 @@ def values_torch(kind: str, seed: int, rank: int, start: int, n: int, device, si
     import torch
 
     idx = torch.arange(start, start + n, dtype=torch.int64, device=device)
-    if kind == "uniform":
+    if kind in ("uniform", "uniform_bf16"):
         k = (u32_torch(seed, rank, idx) >> 8) - (1 << 23)
-        return k.to(torch.float32) * (2.0 ** -23)
+        x = k.to(torch.float32) * (2.0 ** -23)
+        return x.to(torch.bfloat16) if kind == "uniform_bf16" else x
     if kind in ("normal", "normal_bf16"):
         K = torch.zeros_like(idx)
         for j in range(12):

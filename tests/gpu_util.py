@@ -11,6 +11,7 @@ import synthetic
 VEC = {ar.AR_FLOAT32: 4, ar.AR_BFLOAT16: 8, ar.AR_INT32: 4}
 TORCH = {ar.AR_FLOAT32: torch.float32, ar.AR_BFLOAT16: torch.bfloat16, ar.AR_INT32: torch.int32}
 KIND_DTYPE = {"uniform": ar.AR_FLOAT32, "normal": ar.AR_FLOAT32, "normal_bf16": ar.AR_BFLOAT16,
+              "uniform_bf16": ar.AR_BFLOAT16,
               "int": ar.AR_INT32}
 GUARD = 64          # bytes of guard words on each side of a guarded buffer
 GUARD_BYTE = 0x5A

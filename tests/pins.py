@@ -500,6 +500,41 @@ def pin_sampled_matches_full(O):
                                full[idx], f"sampled P={P} dtype={dtype} algo={algo} op={op}")
 
 
+def pin_large_counts_match_small_problems(O):
+    """Counts past 2^31, 2^32 and 2^33 elements.  Element e's fold depends on
+    e only through its ring chunk e // L (L = roundup(ceil(count / P), V)) or
+    its tree (e < H), so the sampled oracle at a huge count must equal the
+    full oracle -- brute-force-pinned above -- on a small problem with the
+    same P values in the same chunk (count P * V, chunk length V) or the same
+    tree (count 2V, split V).  Catches 32-bit overflow in the chunk length, the
+    chunk index or the split."""
+    rng = np.random.default_rng(31)
+    for P, count, dtype in ((3, 2 ** 31 + 2 ** 20 + 3, F32), (2, 2 ** 32 + 13, BF16), (9, 2 ** 31 + 9, BF16),
+                            (8, 2 ** 33 + 5, F32), (72, 2 ** 32 + 1, I32)):
+        V = 8 if dtype == BF16 else 4
+        L = -(-(-(-count // P)) // V) * V
+        H = min(count, -(-(-(-count // 2)) // V) * V)
+        pts = {0, count - 1, 2 ** 31 - 1, 2 ** 31, 2 ** 32 - 1, 2 ** 32, H - 1, H, H + 1}
+        pts |= {c * L + d for c in range(P + 1) for d in (-1, 0, 1)}
+        pts |= set(rng.integers(0, count, 10).tolist())
+        idx = np.array(sorted(i for i in pts if 0 <= i < count), dtype=np.uint64)
+        vals = np.stack(random_inputs(rng, P, len(idx), dtype))
+        for op, scale in ((SUM, 1.0 if dtype == I32 else 0.5), (MAX, 1.0)):
+            for algo in (RING, TREE):
+                got = O.allreduce_sampled(vals, idx, count, dtype, op, algo, scale)
+                for i, e in enumerate(idx.tolist()):
+                    if algo == RING:
+                        n, pos = P * V, (e // L) * V
+                    else:
+                        n, pos = 2 * V, 0 if e < H else V
+                    small = [np.zeros(n, dtype=NP_DTYPE[dtype]) for _ in range(P)]
+                    for r in range(P):
+                        small[r][pos] = vals[r, i]
+                    want = O.allreduce(small, dtype, op, algo, scale)[0][pos]
+                    assert_bitwise(np.array([got[i]]), np.array([want]),
+                                   f"P={P} count={count} e={e} algo={algo} op={op}")
+
+
 # ------------------------------------------- reduce-scatter and all-gather
 
 def _golden(name):
@@ -726,4 +761,5 @@ ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_
             pin_sampled_matches_full, pin_reduce_scatter_worked_example, pin_all_gather_worked_example,
             pin_allreduce_is_reduce_scatter_then_all_gather, pin_reduce_scatter_ring_steps,
             pin_collectives_order_independent, pin_hierarchical_steps,
-            pin_hierarchical_degenerate_is_ring, pin_hierarchical_order_independent]
+            pin_hierarchical_degenerate_is_ring, pin_hierarchical_order_independent,
+            pin_large_counts_match_small_problems]

@@ -58,6 +58,10 @@ MUTANTS = {
                           "    size_t L2 = round_up((count + (size_t)G - 1) / (size_t)G, V);"),
     "ag_wrong_offset": ("memcpy((char*)recv[r] + ((size_t)s * sendcount + i) * es,",
                         "memcpy((char*)recv[r] + ((size_t)((s + r) % P) * sendcount + i) * es,"),
+    # 32-bit slips that only show at counts past 2^32 elements
+    "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
+    "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
+                         "size_t h = round_up((size_t)(uint32_t)(count + 1) / 2, vec_elems(dtype));"),
 }
 
 
