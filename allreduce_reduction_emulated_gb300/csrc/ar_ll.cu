@@ -13,8 +13,8 @@
 //            (x_g, x_{g+1}, ...) -- so LL == RING bit for bit -- and writes
 //            the result straight into all P receive buffers (the all-gather).
 // A new epoch per call means the staging area is never cleared between calls;
-// the epoch is kept on the device (ll_epoch_begin / ll_epoch_end), so a call
-// can be captured in a CUDA graph.  All blocks must be resident at once (a
+// the epoch is kept on the device (ll_epoch_begin / ll_epoch_arrive /
+// ll_epoch_end), so a call can be captured in a CUDA graph.  All blocks must be resident at once (a
 // reducer waits for other blocks), so the kernel is launched cooperatively;
 // every flag wait is bounded, and on its limit the thread records
 // AR_ERR_TIMEOUT in the status word and stops reducing.
@@ -150,15 +150,23 @@ __global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_c
   const int g = blockIdx.x / p.bpr;
   const uint64_t lt = (uint64_t)(blockIdx.x % p.bpr) * kLLThreads + threadIdx.x;
   const uint64_t nt = (uint64_t)p.bpr * kLLThreads;
+  // the first payload word is loaded while thread 0 reads the epoch
+  const bool first = !p.skip_produce && lt < p.nwords;
+  const uint32_t w0 = first ? load_payload(p.send[g], lt, p.nbytes) : 0u;
   const uint32_t epoch = ll_epoch_begin(p.epoch_state);
   const unsigned long long tag = (unsigned long long)epoch << 32;
 
   // produce: stage rank g's payload words with this call's flag
   if (!p.skip_produce) {
     unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
-    for (uint64_t w = lt; w < p.nwords; w += nt)
+    if (first) st_relaxed_u64(slot + lt, tag | w0);
+    for (uint64_t w = lt + nt; w < p.nwords; w += nt)
       st_relaxed_u64(slot + w, tag | load_payload(p.send[g], w, p.nbytes));
   }
+  // counted in by the block's last thread, off the reducers' path: with
+  // chunks of fewer than 256 words (up to 8 KiB per rank at P = 8) it has
+  // nothing to reduce
+  if (threadIdx.x == kLLThreads - 1) ll_epoch_arrive(p.epoch_state, epoch);
   ll_reduce_chunk<MAXP, DT, OP>(p, g, lt, nt, epoch);
   ll_epoch_end(p.epoch_state, epoch, p.staging, p.stage_words);
 }

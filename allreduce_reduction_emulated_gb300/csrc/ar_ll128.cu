@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) ll128_allreduce_kernel(const __grid_
     }
   }
 
+  if (threadIdx.x == kThreads - 1) ll_epoch_arrive(p.epoch_state, epoch);
   ll128_reduce_chunk<MAXP, DT, OP>(p, g, flag);
   ll_epoch_end(p.epoch_state, epoch, p.staging, p.stage_words);
 }

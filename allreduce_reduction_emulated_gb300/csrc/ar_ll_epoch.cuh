@@ -4,7 +4,7 @@
 // lives on the device, so a call carries no host state and can be captured
 // in a CUDA graph and replayed: state[0] is the last epoch used (0: none
 // since the staging area was last cleared, and 0 is never a live flag),
-// state[1] counts the blocks of the running call that have finished.
+// state[1] counts the blocks of the running call that have read it.
 #pragma once
 
 #include "ar_device.cuh"
@@ -21,6 +21,8 @@ __device__ __forceinline__ void st_relaxed_u32(unsigned int* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+constexpr uint32_t kLLEpochWrap = 0xffffffffu;  // the last 32-bit epoch
+
 // Every block reads the last epoch before doing anything; this call uses
 // the next one.
 __device__ __forceinline__ uint32_t ll_epoch_begin(const unsigned int* state) {
@@ -30,13 +32,30 @@ __device__ __forceinline__ uint32_t ll_epoch_begin(const unsigned int* state) {
   return s_epoch;
 }
 
+// Called by ONE thread of each block, any time after ll_epoch_begin (the
+// barrier there orders the block's read of state[0] before this thread's
+// fence).  The block that completes the count publishes the epoch at once:
+// every block has read the old value by then, and the next call starts only
+// after this kernel ends, so the publication need not wait for the other
+// blocks to finish.  The wrap epoch is counted in ll_epoch_end instead.
+__device__ __forceinline__ void ll_epoch_arrive(unsigned int* state, uint32_t epoch) {
+  if (epoch == kLLEpochWrap) return;
+  __threadfence();
+  if (atomicAdd(&state[1], 1u) == gridDim.x - 1) {
+    __threadfence();
+    st_relaxed_u32(&state[1], 0u);
+    st_relaxed_u32(&state[0], epoch);
+  }
+}
+
 // Called by every thread of every block once the block is done with the
-// staging area.  The last block to finish publishes the epoch, after every
-// block has read the old value at its start; when the last 32-bit value has
-// been used it first clears the whole staging area (`words` 8-byte words),
-// so that numbering can restart at 1 without old words matching.
+// staging area; it does work only for the wrap epoch.  When the last 32-bit
+// value has been used, the last block to finish clears the whole staging
+// area (`words` 8-byte words) and then resets the epoch to 0, so that
+// numbering can restart at 1 without old words matching.
 __device__ __forceinline__ void ll_epoch_end(unsigned int* state, uint32_t epoch,
                                              unsigned long long* staging, uint64_t words) {
+  if (epoch != kLLEpochWrap) return;  // counted in by ll_epoch_arrive
   __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -46,15 +65,12 @@ __device__ __forceinline__ void ll_epoch_end(unsigned int* state, uint32_t epoch
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const bool wrap = epoch == 0xffffffffu;
-  if (wrap) {
-    for (uint64_t i = threadIdx.x; i < words; i += blockDim.x) st_relaxed_u64(staging + i, 0ull);
-    __threadfence();
-    __syncthreads();
-  }
+  for (uint64_t i = threadIdx.x; i < words; i += blockDim.x) st_relaxed_u64(staging + i, 0ull);
+  __threadfence();
+  __syncthreads();
   if (threadIdx.x == 0) {
     st_relaxed_u32(&state[1], 0u);
-    st_relaxed_u32(&state[0], wrap ? 0u : epoch);
+    st_relaxed_u32(&state[0], 0u);
   }
 }
 
