@@ -149,9 +149,10 @@ def parse_args():
                          "bucketed all-reduce: compute, comm, serial and overlapped step times")
     ap.add_argument("--tokens", type=int, default=512,
                     help="tokens per rank for --ddp-overlap's gradient GEMMs")
-    ap.add_argument("--comm-blocks", type=int, default=0,
+    ap.add_argument("--comm-blocks", type=lambda v: v if v == "auto" else int(v), default=0,
                     help="--ddp-overlap: cap the all-reduce kernels at this many thread blocks (0 = none); "
-                         "below the SM count they run the TMA pipeline, one block per SM (48 measured best)")
+                         "below the SM count they run the TMA pipeline, one block per SM (48 measured best; "
+                         "'auto' = that share of this GPU's SMs)")
     ap.add_argument("--grad-dtype", choices=("fp32", "bf16"), default="fp32",
                     help="--ddp-overlap: gradient dtype (bf16: bf16 GEMMs and bf16 bucket all-reduces)")
     ap.add_argument("--comm-priority", action="store_true",
@@ -842,6 +843,7 @@ def ddp_overlap(args):
     high = torch.cuda.Stream.priority_range()[1] if args.comm_priority else 0
     reducer = BucketReducer(comm, grads, B, scale=0.125, out=outs, stream=torch.cuda.Stream(priority=high),
                             max_blocks=args.comm_blocks)
+    comm_blocks = reducer.max_blocks
     torch.cuda.synchronize()                    # inputs made on the default stream
 
     def backward(overlap):
@@ -897,7 +899,7 @@ def ddp_overlap(args):
                        f"{(total + B - 1) // B} x 25 MiB buckets, ring, scale 1/8",
         "grad_dtype": args.grad_dtype,
         "tokens_per_rank": T, "steps": args.steps, "unit": "ms",
-        "comm_blocks": args.comm_blocks, "comm_priority": bool(args.comm_priority),
+        "comm_blocks": comm_blocks, "comm_priority": bool(args.comm_priority),
         "compute_ms": times["compute"], "comm_ms": times["comm"], "serial_ms": times["serial"],
         "overlap_ms": times["overlap"], "exposed_comm_ms": times["overlap"] - times["compute"],
         "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,

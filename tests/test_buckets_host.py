@@ -81,3 +81,23 @@ def test_out_buffers_receive_the_results(recorder):
     red = B.BucketReducer(comm=1, grads=grads, bucket=4, out=outs, stream=FakeStream())
     red.ready(10, "e")
     assert [c[2] - outs[0].data_ptr() for c in recorder] == [0, 16, 32]
+
+
+def test_auto_cap_is_the_measured_share_of_the_sms(recorder, monkeypatch):
+    class Props:
+        multi_processor_count = 152
+
+    monkeypatch.setattr(B.torch.cuda, "get_device_properties", lambda device: Props)
+    red, _, _ = make(max_blocks="auto")
+    assert red.max_blocks == 48
+    red.ready(1000, "e")
+    assert all(c[2] == 48 for c in recorder if c[0] == "option")
+    Props.multi_processor_count = 132
+    assert B.auto_max_blocks("cuda:0") == 42
+    Props.multi_processor_count = 1
+    assert B.auto_max_blocks("cuda:0") == 1
+
+
+def test_bad_cap_rejected():
+    with pytest.raises(ValueError):
+        make(max_blocks="most")

@@ -31,9 +31,10 @@ def dev():
 
 
 @pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
-@pytest.mark.parametrize("max_blocks", [None, 16])
+@pytest.mark.parametrize("max_blocks", [None, 16, "auto"])
 def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks, gdt):
-    """max_blocks=16: the bucket all-reduces run on 16 SMs (the TMA pipeline).
+    """max_blocks=16 or "auto" (48 of 152 SMs): the bucket all-reduces run on a
+    few SMs (the TMA pipeline).
     bf16: bf16 GEMMs write bf16 gradients, reduced with fp32 accumulation."""
     P, T, bucket = 4, 96, 300_000
     shapes = [(512, 1024), (1024, 512), (512, 768)] * 2          # 6 "parameters", backward order
