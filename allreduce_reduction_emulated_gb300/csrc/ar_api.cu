@@ -1,6 +1,8 @@
 // ar_api.cu -- the C ABI of libar.so (declared in include/ar.h): communicator
 // lifetime, argument checks, algorithm selection and kernel dispatch.
-// Host code only; the kernels live in ar_static_*.cu, ar_generic.cu, ar_ll.cu.
+// Host code only; the kernels live in ar_static_*.cu and ar_tma_*.cu (P <= 8,
+// on the whole GPU and on a few SMs), ar_generic.cu (any P), ar_ll.cu,
+// ar_ll128.cu, ar_collectives.cu and ar_tma_gather.cu.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>

@@ -2,8 +2,10 @@
 // collectives ("NCCL, NIXL, and Distributed GPU Communication", sections
 // "Reduce-scatter" and "All-gather"):
 //   reduce-scatter -- element-wise kernel for shards that are not whole
-//                     16-byte vectors (the vector case runs the pipelined
-//                     ring kernel in ar_generic.cu);
+//                     16-byte vectors (whole-vector shards run the ring
+//                     kernels in scatter mode: ar_static.cuh for P <= 8,
+//                     ar_tma.cuh when capped to a few SMs, ar_generic.cu
+//                     above 8 ranks);
 //   all-gather     -- rank s's sendcount elements copied to offset
 //                     s * sendcount of every rank's receive buffer: one read
 //                     and P writes per element, 16-byte vectors when every
