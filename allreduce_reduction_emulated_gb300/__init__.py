@@ -258,6 +258,11 @@ def allreduce(sends, recvs=None, op: str = "sum", algo: str = "auto", scale: flo
     """
     import torch
 
+    if op not in OPS or algo not in ALGOS:
+        raise ArError(AR_ERR_INVALID_ARG, f"allreduce: op must be one of {sorted(OPS)}, "
+                                          f"algo one of {sorted(ALGOS)}")
+    if len(sends) == 0:
+        raise ArError(AR_ERR_INVALID_ARG, "allreduce: no tensors")
     recvs = list(sends) if recvs is None else list(recvs)
     t0 = sends[0]
     for t in list(sends) + recvs:

@@ -136,3 +136,19 @@ def test_binding_checks_length_and_element_size(monkeypatch):
     with pytest.raises(ar.ArError) as e:
         ar._ptrs([CudaLike(torch.zeros(15))], 2 * 8, ar.AR_FLOAT32, "x")
     assert "15 elements, 16 needed" in str(e.value)
+
+
+def test_convenience_call_rejects_bad_names_and_empty_input():
+    import torch
+
+    x = torch.zeros(8)
+    for kw, reason in ((dict(op="avg"), "op must be one of"), (dict(algo="nvls"), "algo one of")):
+        with pytest.raises(ar.ArError) as e:
+            ar.allreduce([x, x], **kw)
+        assert e.value.status == ar.AR_ERR_INVALID_ARG and reason in str(e.value)
+    with pytest.raises(ar.ArError) as e:
+        ar.allreduce([])
+    assert "no tensors" in str(e.value)
+    with pytest.raises(ar.ArError) as e:
+        ar.allreduce([x, x])                       # CPU tensors: refused before the library
+    assert "contiguous CUDA tensors" in str(e.value)
