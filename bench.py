@@ -153,6 +153,9 @@ def parse_args():
                     help="--ddp-overlap: cap the all-reduce kernels at this many thread blocks (0 = none); "
                          "below the SM count they run the TMA pipeline, one block per SM (48 measured best; "
                          "'auto' = that share of this GPU's SMs)")
+    ap.add_argument("--gemm-carveout", type=int, default=0,
+                    help="--ddp-overlap: leave this many SMs out of the gradient GEMMs (PyTorch's "
+                         "experimental cuBLAS SM carve-out; 0 = none)")
     ap.add_argument("--grad-dtype", choices=("fp32", "bf16"), default="fp32",
                     help="--ddp-overlap: gradient dtype (bf16: bf16 GEMMs and bf16 bucket all-reduces)")
     ap.add_argument("--comm-priority", action="store_true",
@@ -845,6 +848,10 @@ def ddp_overlap(args):
                             max_blocks=args.comm_blocks)
     comm_blocks = reducer.max_blocks
     torch.cuda.synchronize()                    # inputs made on the default stream
+    if args.gemm_carveout:
+        if not hasattr(torch._C, "_set_sm_carveout_experimental"):
+            raise SystemExit("--gemm-carveout: this PyTorch has no SM carve-out")
+        torch._C._set_sm_carveout_experimental(args.gemm_carveout)
 
     def backward(overlap):
         for vs, m, n, end in views:
@@ -900,6 +907,7 @@ def ddp_overlap(args):
         "grad_dtype": args.grad_dtype,
         "tokens_per_rank": T, "steps": args.steps, "unit": "ms",
         "comm_blocks": comm_blocks, "comm_priority": bool(args.comm_priority),
+        "gemm_carveout": args.gemm_carveout,
         "compute_ms": times["compute"], "comm_ms": times["comm"], "serial_ms": times["serial"],
         "overlap_ms": times["overlap"], "exposed_comm_ms": times["overlap"] - times["compute"],
         "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,
