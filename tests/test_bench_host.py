@@ -114,3 +114,17 @@ def test_clock_summary_reads_nvidia_smi_rows():
     c.rows.append((3.0, ["0", "[N/A]"]))
     s = c.summary(100.0, 101.0)
     assert s["samples_in_timed_region"] == 0 and s["samples"] == 7 and s["sm_mhz"] == 2017.5  # median of 6
+
+
+def test_overlap_arguments(monkeypatch):
+    monkeypatch.setattr("sys.argv", ["bench.py", "--ddp-overlap", "--comm-blocks", "auto", "--gemm-carveout", "32",
+                                     "--grad-dtype", "bf16", "--comm-priority"])
+    a = bench.parse_args()
+    assert (a.ddp_overlap, a.comm_blocks, a.gemm_carveout, a.grad_dtype, a.comm_priority) == \
+        (True, "auto", 32, "bf16", True)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--ddp-overlap", "--comm-blocks", "48"])
+    a = bench.parse_args()
+    assert (a.comm_blocks, a.gemm_carveout, a.grad_dtype) == (48, 0, "fp32")
+    monkeypatch.setattr("sys.argv", ["bench.py", "--comm-blocks", "most"])
+    with pytest.raises(SystemExit):
+        bench.parse_args()
