@@ -896,6 +896,18 @@ def ddp_overlap(args):
         b.record()
         torch.cuda.synchronize()
         times[kind] = a.elapsed_time(b) / args.steps
+    # where the overlapped step's time goes: one eager run with events at the
+    # step start, after the last GEMM and after the last bucket's all-reduce
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(compute):
+        reducer.reset()
+        marks[0].record(compute)
+        backward(True)
+        marks[1].record(compute)
+        compute.wait_event(reducer.finish())
+        marks[2].record(compute)
+    torch.cuda.synchronize()
+    gemm_end, step_end = marks[0].elapsed_time(marks[1]), marks[0].elapsed_time(marks[2])
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error")
     ar.ar_destroy(comm)
@@ -913,6 +925,10 @@ def ddp_overlap(args):
         "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,
         "hidden_fraction_of_shorter": (times["serial"] - times["overlap"]) / min(times["compute"], times["comm"]),
         "gemm_tflops": flops / (times["compute"] * 1e-3) / 1e12,
+        "eager_overlap": {"last_gemm_end_ms": gemm_end, "step_end_ms": step_end,
+                          "after_last_gemm_ms": step_end - gemm_end,
+                          "buckets_after_last_gemm_at_comm_rate":
+                              (step_end - gemm_end) / (times["comm"] / len(reducer.starts))},
         "comm_hbm_gbs": 2 * P * total * esize / (times["comm"] * 1e-3) / 1e9,
     }), flush=True)
 
