@@ -897,10 +897,13 @@ def ddp_overlap(args):
         torch.cuda.synchronize()
         times[kind] = a.elapsed_time(b) / args.steps
     # where the overlapped step's time goes: one eager run with events at the
-    # step start, after the last GEMM and after the last bucket's all-reduce
+    # step start, after the last GEMM and after the last bucket's all-reduce;
+    # a 100 ms spin holds the GPU while the host enqueues the step, so the
+    # host's issue rate does not set the pace
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     with torch.cuda.stream(compute):
         reducer.reset()
+        torch.cuda._sleep(int(2e8))
         marks[0].record(compute)
         backward(True)
         marks[1].record(compute)
