@@ -29,7 +29,7 @@ struct ar_comm {
   int skip_produce = 0;
   int debug = 0;
   // device control block (kControlInts ints): [0] the ar_status_t word,
-  // [2..3] LL epoch state, [4..5] LL128 epoch state ({last epoch, finished blocks})
+  // [2..3] LL epoch state, [4..5] LL128 epoch state ({last epoch, blocks counted in})
   int* status = nullptr;
   int16_t* tree_push = nullptr;  // device: tree 0's then tree 1's ranks in preorder (P each)
   // LL128 staging: P slots of `ll128_stride` 8-byte words (128-byte lines)

@@ -153,8 +153,9 @@ def test_epoch_option_arguments(dev):
 
 
 def test_many_back_to_back_calls(dev):
-    """20,000 LL / LL128 calls in a row on one stream, sizes changing: each
-    call's last block publishes the epoch the next call starts from.  Checked
+    """20,000 LL / LL128 calls in a row on one stream, sizes changing: in each
+    call the block that completes the count publishes the epoch the next call
+    starts from.  Checked
     against the ring every few hundred calls and for the device status."""
     P = 8
     comm = ar.ar_init(P)
