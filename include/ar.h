@@ -73,8 +73,10 @@
 extern "C" {
 #endif
 
-/* Opaque communicator.  Created once and reused ("NCCL, NIXL, ...", checklist
- * item "NCCL communicator ... must not be created inside the loop"). */
+/* Opaque communicator.  Created once and reused across calls: creating one is
+ * expensive, so it belongs outside the training loop ("NCCL, NIXL, and
+ * Distributed GPU Communication", the checklist item on communicator
+ * creation). */
 typedef struct ar_comm* ar_comm_t;
 
 typedef enum {
