@@ -282,6 +282,18 @@ def profiled_traffic(workload: str):
 
 # ------------------------------------------------------------ aggregation
 
+def sm_time_bound_ms(compute_ms: float, comm_ms: float, comm_sms: int, sms: int):
+    """Lower bound on an overlapped step when both sides are SM-bound: the
+    GEMMs need compute_ms on all `sms` SMs, the all-reduces comm_ms on
+    `comm_sms` of them, and the step can be no shorter than their SM-time
+    spread over the whole GPU (nor than either side alone).  None when the
+    all-reduces are not capped (they then take whole SMs from the GEMMs in
+    turns, and the split is not known)."""
+    if not comm_sms or comm_sms >= sms:
+        return None
+    return max((compute_ms * sms + comm_ms * comm_sms) / sms, compute_ms, comm_ms)
+
+
 def max_over_ranks(x: float, dist=None) -> float:
     """The slowest rank's time (every rank gets it)."""
     if dist is None:
@@ -926,6 +938,8 @@ def ddp_overlap(args):
         "compute_ms": times["compute"], "comm_ms": times["comm"], "serial_ms": times["serial"],
         "overlap_ms": times["overlap"], "exposed_comm_ms": times["overlap"] - times["compute"],
         "max_compute_comm_ms": model, "tail_ms": times["overlap"] - model,
+        "sm_time_bound_ms": sm_time_bound_ms(times["compute"], times["comm"], comm_blocks or 0,
+                                             torch.cuda.get_device_properties(dev).multi_processor_count),
         "hidden_fraction_of_shorter": (times["serial"] - times["overlap"]) / min(times["compute"], times["comm"]),
         "gemm_tflops": flops / (times["compute"] * 1e-3) / 1e12,
         "eager_overlap": {"last_gemm_end_ms": gemm_end, "step_end_ms": step_end,

@@ -128,3 +128,11 @@ def test_overlap_arguments(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py", "--comm-blocks", "most"])
     with pytest.raises(SystemExit):
         bench.parse_args()
+
+
+def test_sm_time_bound():
+    # 18.4 ms of GEMMs on 152 SMs + 17.0 ms of all-reduce on 48: 23.77 ms
+    assert bench.sm_time_bound_ms(18.4, 17.0, 48, 152) == pytest.approx(18.4 + 17.0 * 48 / 152)
+    assert bench.sm_time_bound_ms(1.0, 30.0, 8, 152) == 30.0          # never below either side
+    assert bench.sm_time_bound_ms(18.4, 11.4, 0, 152) is None          # uncapped: split unknown
+    assert bench.sm_time_bound_ms(18.4, 11.4, 152, 152) is None
