@@ -294,6 +294,24 @@ def sm_time_bound_ms(compute_ms: float, comm_ms: float, comm_sms: int, sms: int)
     return max((compute_ms * sms + comm_ms * comm_sms) / sms, compute_ms, comm_ms)
 
 
+PG_TIMEOUT_S = 600  # rank 0 builds the library while the other ranks wait at the first barrier
+
+
+def init_replicas(world: int, rank: int, timeout_s: float = PG_TIMEOUT_S):
+    """The gloo process group of N independent replicas (it carries only the
+    host-side barriers and the max over ranks of the timings).  A rank that
+    exits makes its peers' next barrier fail at once; one that never arrives
+    makes it fail after timeout_s, instead of blocking them."""
+    import datetime
+
+    import torch.distributed as dist
+
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=timeout_s))
+    return dist
+
+
 def max_over_ranks(x: float, dist=None) -> float:
     """The slowest rank's time (every rank gets it)."""
     if dist is None:
@@ -437,12 +455,7 @@ def ours_arm(args, w, name):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist = init_replicas(world, rank) if world > 1 else None
     if rank == 0:
         __graft_entry__.build()
     if dist:

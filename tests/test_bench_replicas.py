@@ -64,3 +64,54 @@ def test_fit_alpha_beta_recovers_a_line():
     alpha, beta = bench.fit_alpha_beta(pts)
     assert alpha == pytest.approx(3e-6, rel=1e-3)
     assert 1 / beta == pytest.approx(500e9, rel=1e-6)
+
+
+def _failing_pair(rank, port, mode, timeout_s, q):
+    """Rank 1 fails in `mode` ("exit": leaves before the barrier; "absent":
+    never reaches it); rank 0 reports what its barrier did and how long it
+    took."""
+    import time
+
+    os.environ["MASTER_PORT"] = str(port)
+    os.environ.pop("MASTER_ADDR", None)
+    d = bench.init_replicas(2, rank, timeout_s=timeout_s)
+    if rank == 1:
+        if mode == "exit":
+            os._exit(3)
+        time.sleep(timeout_s * 4)        # absent: the parent ends this process
+        os._exit(0)
+    t0 = time.monotonic()
+    try:
+        d.barrier()
+        q.put(("completed", time.monotonic() - t0))
+    except Exception as exc:             # gloo reports a lost or silent peer as an error
+        q.put((type(exc).__name__, time.monotonic() - t0))
+    q.close()
+    q.join_thread()                      # the result is sent before the process ends
+    os._exit(0)
+
+
+@pytest.mark.parametrize("mode", ["exit", "absent"])
+def test_a_failed_replica_ends_the_others_barrier(mode):
+    """Failure detection on the host: the surviving rank's barrier ends with
+    an error -- at once when the peer exits, after the process group's
+    timeout when it never arrives -- and never blocks."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port, timeout_s = _free_port(), 5
+    procs = [ctx.Process(target=_failing_pair, args=(r, port, mode, timeout_s, q)) for r in (0, 1)]
+    for p in procs:
+        p.start()
+    try:
+        outcome, seconds = q.get(timeout=120)
+    finally:
+        for p in procs:
+            p.join(timeout=1)
+            if p.is_alive():
+                p.kill()                 # this test's own child, by its handle
+                p.join(timeout=10)
+    assert outcome != "completed"
+    if mode == "exit":
+        assert seconds < timeout_s               # the lost connection is seen at once
+    else:
+        assert timeout_s * 0.5 <= seconds < timeout_s * 3
