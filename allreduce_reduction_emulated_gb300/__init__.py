@@ -238,6 +238,7 @@ def ar_allreduce_ll_noalloc(sendbufs, recvbufs, count: int, dtype: int, op: int 
 # ------------------------------------------------------------- convenience
 
 _comms: dict = {}
+_comms_lock = threading.Lock()
 
 
 def dtype_of(t) -> int:
@@ -270,9 +271,10 @@ def allreduce(sends, recvs=None, op: str = "sum", algo: str = "auto", scale: flo
             raise ArError(AR_ERR_INVALID_ARG, "allreduce: tensors must be contiguous CUDA tensors "
                                               "of one dtype and size")
     key = (len(sends), t0.device.index if t0.device.index is not None else torch.cuda.current_device())
-    if key not in _comms:
-        with torch.cuda.device(key[1]):
-            _comms[key] = ar_init(len(sends))
+    with _comms_lock:
+        if key not in _comms:
+            with torch.cuda.device(key[1]):
+                _comms[key] = ar_init(len(sends))
     with torch.cuda.device(key[1]):
         ar_allreduce(_comms[key], sends, recvs, t0.numel(), dtype_of(t0), OPS[op], ALGOS[algo],
                      scale, stream)
