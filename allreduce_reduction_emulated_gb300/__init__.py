@@ -255,7 +255,9 @@ def allreduce(sends, recvs=None, op: str = "sum", algo: str = "auto", scale: flo
     """All-reduce of P same-shaped contiguous CUDA tensors; returns recvs.
 
     recvs=None reduces in place.  A communicator per (P, device) is created on
-    first use and kept for the life of the process.
+    first use and kept for the life of the process; calls that share it must
+    not overlap on the GPU (one stream, or streams ordered by events), as for
+    any communicator.
     """
     import torch
 
