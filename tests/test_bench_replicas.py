@@ -74,14 +74,18 @@ def _failing_pair(rank, port, mode, timeout_s, q):
 
     os.environ["MASTER_PORT"] = str(port)
     os.environ.pop("MASTER_ADDR", None)
-    d = bench.init_replicas(2, rank, timeout_s=timeout_s)
     if rank == 1:
+        bench.init_replicas(2, rank, timeout_s=timeout_s)
         if mode == "exit":
             os._exit(3)
         time.sleep(timeout_s * 4)        # absent: the parent ends this process
         os._exit(0)
     t0 = time.monotonic()
     try:
+        # an early exit of rank 1 may already fail the set-up; that too is
+        # the failure seen, not a hang
+        d = bench.init_replicas(2, rank, timeout_s=timeout_s)
+        t0 = time.monotonic()
         d.barrier()
         q.put(("completed", time.monotonic() - t0))
     except Exception as exc:             # gloo reports a lost or silent peer as an error
