@@ -279,7 +279,9 @@ def pin_ring_simulation(O, quick: bool = False):
             for dtype in (F32, BF16, I32):
                 sends = random_inputs(rng, P, count, dtype)
                 for op in (SUM, MIN, MAX):
-                    scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                    # 1/P: the DDP mean, not a power of two for most P, so scaling
+                    # the inputs instead of the result would show
+                    scales = (1.0, 0.125, 1.0 / P, 0.1) if (op == SUM and dtype != I32) else (1.0,)
                     for scale in scales:
                         want = ring_message_passing(sends, dtype, op, scale)
                         for algo in (RING, LL):
@@ -635,7 +637,7 @@ def pin_reduce_scatter_ring_steps(O):
             for dtype in (F32, BF16, I32):
                 sends = random_inputs(rng, P, P * rc, dtype)
                 for op in (SUM, MIN, MAX):
-                    scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                    scales = (1.0, 0.125, 1.0 / P, 0.1) if (op == SUM and dtype != I32) else (1.0,)
                     for scale in scales:
                         want = ring_reduce_scatter_steps(sends, dtype, op, scale)
                         got = O.reduce_scatter(sends, dtype, op, scale)
@@ -710,7 +712,7 @@ def pin_hierarchical_steps(O, quick: bool = False):
             for dtype in (F32, BF16, I32):
                 sends = random_inputs(rng, P, count, dtype)
                 for op in (SUM, MIN, MAX):
-                    scales = (1.0, 0.125) if (op == SUM and dtype != I32) else (1.0,)
+                    scales = (1.0, 0.125, 1.0 / P, 0.1) if (op == SUM and dtype != I32) else (1.0,)
                     for scale in scales:
                         want = hierarchical_steps(sends, Q, dtype, op, scale)
                         got = O.allreduce_hier(sends, Q, dtype, op, scale)

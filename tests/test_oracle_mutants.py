@@ -58,6 +58,21 @@ MUTANTS = {
                           "    size_t L2 = round_up((count + (size_t)G - 1) / (size_t)G, V);"),
     "ag_wrong_offset": ("memcpy((char*)recv[r] + ((size_t)s * sendcount + i) * es,",
                         "memcpy((char*)recv[r] + ((size_t)((s + r) % P) * sendcount + i) * es,"),
+    "scale_before_fold": ("    acc_t acc;\n    if (algo == OR_ALGO_TREE) {",
+                          "    acc_t xs[OR_MAX_RANKS];\n"
+                          "    for (int r = 0; r < P; ++r) {\n"
+                          "        xs[r] = x[r];\n"
+                          "        if (dtype != OR_I32 && scale != 1.0f) xs[r].f = xs[r].f * scale;\n"
+                          "    }\n"
+                          "    x = xs;\n    scale = 1.0f;\n"
+                          "    acc_t acc;\n    if (algo == OR_ALGO_TREE) {"),
+    "bf16_truncate": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;", "(void)lower;"),
+    "int_sum_saturates": ("if (op == OR_SUM) acc.u = acc.u + x.u; /* wraps modulo 2^32 */",
+                          "if (op == OR_SUM) {\n"
+                          "            int64_t s = (int64_t)(int32_t)acc.u + (int64_t)(int32_t)x.u;\n"
+                          "            acc.u = (uint32_t)(int32_t)(s > INT32_MAX ? INT32_MAX : s < INT32_MIN ? INT32_MIN : s);\n"
+                          "        }"),
+    "tree_root_below_p": ("    while (r * 2 <= P) r *= 2;", "    while (r * 2 < P) r *= 2;"),
     # 32-bit slips that only show at counts past 2^32 elements
     "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
     "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
