@@ -73,6 +73,21 @@ MUTANTS = {
                           "            acc.u = (uint32_t)(int32_t)(s > INT32_MAX ? INT32_MAX : s < INT32_MIN ? INT32_MIN : s);\n"
                           "        }"),
     "tree_root_below_p": ("    while (r * 2 <= P) r *= 2;", "    while (r * 2 < P) r *= 2;"),
+    "hier_groups_reversed": ("        int g = (int)((c2 + (size_t)j) % (size_t)G);",
+                             "        int g = (int)((c2 + (size_t)(G - j)) % (size_t)G);"),
+    "hier_group_size_swapped": ("    int G = P / Q;", "    int G = Q;\n    Q = P / G;"),
+    "hier_scale_per_group": ("        total = j == 0 ? part : combine(total, part, dtype, op);\n    }\n"
+                             "    if (dtype != OR_I32 && scale != 1.0f) total.f = total.f * scale;\n",
+                             "        if (dtype != OR_I32 && scale != 1.0f) part.f = part.f * scale;\n"
+                             "        total = j == 0 ? part : combine(total, part, dtype, op);\n    }\n"),
+    "float_min_on_bits": ("else if (op == OR_MIN) acc.f = (x.f < acc.f) ? x.f : acc.f;",
+                          "else if (op == OR_MIN) acc.u = (x.u < acc.u) ? x.u : acc.u;"),
+    "ll_folds_as_tree": ("    if (algo == OR_ALGO_TREE) {\n        int t = e",
+                         "    if (algo != OR_ALGO_RING) {\n        int t = e"),
+    "sampled_ignores_idx": ("acc_t y = reduce_element(x, P, count, idx[i], dtype, op, algo, scale);",
+                            "acc_t y = reduce_element(x, P, count, i, dtype, op, algo, scale);"),
+    "hier_sampled_ignores_idx": ("reduce_element_hier(x, P, Q, count, idx[i], dtype, op, scale)",
+                                 "reduce_element_hier(x, P, Q, count, i, dtype, op, scale)"),
     # 32-bit slips that only show at counts past 2^32 elements
     "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
     "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
