@@ -502,6 +502,33 @@ def pin_sampled_matches_full(O):
                                full[idx], f"sampled P={P} dtype={dtype} algo={algo} op={op}")
 
 
+def pin_chunk_and_split_boundaries(O):
+    """Where each element's fold starts, made visible.  Ranks 0..3 hold 2^24,
+    1, 1, -2^24 (exact in fp32 and bf16).  Folded from rank 0 (ring chunk 0)
+    the two 1s are absorbed by 2^24 and the result is 0; from rank 1, 2 or 3
+    it is 2.  Tree 0 (x3 + ((x1 + x0) + x2)) gives 0, tree 1
+    (x0 + ((x2 + x1) + x3)) gives 2.  So the output marks the end of ring
+    chunk 0 and the tree split, which must sit on 16-byte boundaries: 4 fp32 or
+    8 bf16 elements.  The expected boundaries below are worked by hand from
+    the chunk rule (P pieces of ceil(count / P) rounded up to a 16-byte
+    multiple) and the split rule (ceil(count / 2) rounded the same way)."""
+    big = np.float32(2 ** 24)
+    cols = np.array([big, 1.0, 1.0, -big], dtype=np.float32)
+    # (dtype, count, end of ring chunk 0, tree split H)
+    cases = ((F32, 40, 12, 20), (BF16, 40, 16, 24), (F32, 10, 4, 8), (BF16, 10, 8, 8),
+             (BF16, 100, 32, 56), (F32, 7, 4, 4), (BF16, 3, 3, 3),
+             (F32, 9, 4, 8), (BF16, 17, 8, 16))           # odd counts: ceil, not floor, of count / 2
+    for dtype, count, c0, H in cases:
+        sends = [np.full(count, v, dtype=np.float32) for v in cols]
+        if dtype == BF16:
+            sends = [bf16_bits_torch(x) for x in sends]
+        for algo, edge in ((RING, c0), (LL, c0), (TREE, H)):
+            y = np.array(widened(O.allreduce(sends, dtype, SUM, algo)[0], dtype), dtype=np.float64)
+            want = np.where(np.arange(count) < edge, 0.0, 2.0)
+            if not np.array_equal(y, want):
+                raise AssertionError(f"boundaries dtype={dtype} count={count} algo={algo}: got {y.tolist()}")
+
+
 def pin_large_counts_match_small_problems(O):
     """Counts past 2^31, 2^32 and 2^33 elements.  Element e's fold depends on
     e only through its ring chunk e // L (L = roundup(ceil(count / P), V)) or
@@ -764,4 +791,4 @@ ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_
             pin_allreduce_is_reduce_scatter_then_all_gather, pin_reduce_scatter_ring_steps,
             pin_collectives_order_independent, pin_hierarchical_steps,
             pin_hierarchical_degenerate_is_ring, pin_hierarchical_order_independent,
-            pin_large_counts_match_small_problems]
+            pin_large_counts_match_small_problems, pin_chunk_and_split_boundaries]

@@ -88,6 +88,17 @@ MUTANTS = {
                             "acc_t y = reduce_element(x, P, count, i, dtype, op, algo, scale);"),
     "hier_sampled_ignores_idx": ("reduce_element_hier(x, P, Q, count, idx[i], dtype, op, scale)",
                                  "reduce_element_hier(x, P, Q, count, i, dtype, op, scale)"),
+    "rs_scale_before_fold": ("            for (int r = 0; r < P; ++r) x[r] = load_widened(send[r], e, dtype);\n"
+                             "            acc_t acc = x[s];",
+                             "            for (int r = 0; r < P; ++r) {\n"
+                             "                x[r] = load_widened(send[r], e, dtype);\n"
+                             "                if (dtype != OR_I32 && scale != 1.0f) x[r].f = x[r].f * scale;\n"
+                             "            }\n"
+                             "            scale = 1.0f;\n"
+                             "            acc_t acc = x[s];"),
+    "ag_rank0_piece_only": ("(const char*)send[s] + i * es, es);", "(const char*)send[0] + i * es, es);"),
+    "vector_of_4_elements": ("static size_t vec_elems(int dtype) { return 16 / elem_size(dtype); }",
+                             "static size_t vec_elems(int dtype) { (void)dtype; return 4; }"),
     # 32-bit slips that only show at counts past 2^32 elements
     "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
     "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
