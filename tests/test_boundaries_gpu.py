@@ -1,0 +1,97 @@
+"""Ring-chunk edges and the tree split on the GPU, made visible by the data.
+
+Ranks 0..3 hold 2^24, 1, 1, -2^24 (exact in fp32 and bf16) and every other
+rank holds 0.  A fold that meets rank 0's 2^24 before the two 1s absorbs them
+and ends at 0; any other order ends at 2.  So each output element shows which
+order folded it, and a chunk edge or tree split off by even one 16-byte vector
+changes whole elements -- which random data, whose fp32 sums are mostly
+exact, rarely shows.  Every element is compared with the oracle, whose own
+edges are pinned by hand-worked boundaries.  The ring chunks and the split
+follow "NCCL, NIXL, and Distributed GPU Communication" (section
+"Reduce-scatter") and "NCCL and NVSHMEM -- two GPU communication models,
+side by side" (the double binary tree).
+"""
+import numpy as np
+import pytest
+import torch
+
+import allreduce_reduction_emulated_gb300 as ar
+import oracle
+import pins
+from gpu_util import to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+COUNTS = (7, 9, 17, 40, 100, 1000, 4099, 65536 + 13)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def crafted(P, count, dtype):
+    vals = [2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)] + [0.0] * (P - 4)
+    sends = [np.full(count, v, dtype=np.float32) for v in vals]
+    if dtype == ar.AR_BFLOAT16:
+        sends = [pins.bf16_bits_torch(x) for x in sends]
+    return sends
+
+
+def check(comm, sends, count, dtype, algo, dev, want, tag):
+    P = len(sends)
+    xs = [to_device(s, dtype, dev) for s in sends]
+    outs = [torch.empty_like(x) for x in xs]
+    ar.ar_allreduce(comm, xs, outs, count, dtype, ar.AR_SUM, algo, 1.0)
+    torch.cuda.synchronize()
+    assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+    for r in (0, P - 1):
+        pins.assert_bitwise(to_host(outs[r]), want[r], f"{tag} rank {r}")
+
+
+@pytest.mark.parametrize("P,Q", [(4, 2), (5, 0), (8, 4), (12, 4), (72, 8)])
+def test_edges_every_algorithm(P, Q, dev):
+    comm = ar.ar_init(P)
+    try:
+        if Q:
+            ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, Q)
+        for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
+            esize = 2 if dtype == ar.AR_BFLOAT16 else 4
+            for count in COUNTS:
+                sends = crafted(P, count, dtype)
+                ring = oracle.allreduce(sends, dtype, oracle.SUM, oracle.RING)
+                tree = oracle.allreduce(sends, dtype, oracle.SUM, oracle.TREE)
+                algos = [(ar.AR_ALGO_RING, ring), (ar.AR_ALGO_TREE, tree)]
+                if count * esize <= 65536:
+                    algos.append((ar.AR_ALGO_LL, ring))
+                if count * esize <= 1 << 20:
+                    algos.append((ar.AR_ALGO_LL128, ring))
+                if Q:
+                    algos.append((ar.AR_ALGO_HIER, oracle.allreduce_hier(sends, Q, dtype, oracle.SUM)))
+                for algo, want in algos:
+                    check(comm, sends, count, dtype, algo, dev, want, f"P={P} dtype={dtype} count={count} algo={algo}")
+    finally:
+        ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P", [4, 8])
+def test_edges_on_a_few_sms(P, dev):
+    """The TMA pipeline (8 SMs): its tiles are loaded rotated per ring chunk,
+    so a chunk edge inside a tile takes the per-element path."""
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 8)
+        for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
+            for count in (65536 + 13, (1 << 20) + 5, 3 * (1 << 20) + 1000):
+                sends = crafted(P, count, dtype)
+                for algo, oalgo in ((ar.AR_ALGO_RING, oracle.RING), (ar.AR_ALGO_TREE, oracle.TREE)):
+                    want = oracle.allreduce(sends, dtype, oracle.SUM, oalgo)
+                    check(comm, sends, count, dtype, algo, dev, want, f"TMA P={P} dtype={dtype} count={count} algo={algo}")
+    finally:
+        ar.ar_destroy(comm)
