@@ -527,6 +527,25 @@ def pin_chunk_and_split_boundaries(O):
             want = np.where(np.arange(count) < edge, 0.0, 2.0)
             if not np.array_equal(y, want):
                 raise AssertionError(f"boundaries dtype={dtype} count={count} algo={algo}: got {y.tolist()}")
+    # Hierarchical order, P = 8 in G = 4 groups of Q = 2: rank 2g holds group g's
+    # value above, rank 2g + 1 holds 0, so group g's partial is that value and
+    # the fold across groups ends at 0 exactly where it starts at group 0 --
+    # sub-chunk 0 of each intra-group chunk.  Chunks: Q pieces of ceil(count / Q)
+    # rounded to 16 bytes; sub-chunks: G pieces of ceil(chunk length / G), rounded.
+    hier_cases = ((F32, 40, [(0, 8), (20, 28)]),     # chunks [0,20) [20,40); sub-chunks of 8
+                  (BF16, 40, [(0, 8), (24, 32)]),    # chunks [0,24) [24,40); sub-chunks of 8
+                  (F32, 33, [(0, 8), (20, 24)]))     # chunks [0,20) [20,33); sub-chunks of 8, then 4
+    for dtype, count, zeros in hier_cases:
+        vals = [cols[0], 0.0, cols[1], 0.0, cols[2], 0.0, cols[3], 0.0]
+        sends = [np.full(count, v, dtype=np.float32) for v in vals]
+        if dtype == BF16:
+            sends = [bf16_bits_torch(x) for x in sends]
+        y = np.array(widened(O.allreduce_hier(sends, 2, dtype, SUM)[0], dtype), dtype=np.float64)
+        want = np.full(count, 2.0)
+        for lo, hi in zeros:
+            want[lo:hi] = 0.0
+        if not np.array_equal(y, want):
+            raise AssertionError(f"hierarchical boundaries dtype={dtype} count={count}: got {y.tolist()}")
 
 
 def pin_large_counts_match_small_problems(O):
@@ -733,7 +752,9 @@ def hierarchical_steps(sends, Q: int, dtype: int, op: int, scale: float):
 
 def pin_hierarchical_steps(O, quick: bool = False):
     rng = np.random.default_rng(61)
-    cases = [(4, 2), (6, 3), (6, 2), (8, 4), (9, 3), (8, 2), (12, 4)] if not quick else [(9, 3), (12, 4)]
+    # quick: (6, 2) puts chunk starts off the sub-chunk grid (G = 3 > 2, so the
+    # group order shows)
+    cases = [(4, 2), (6, 3), (6, 2), (8, 4), (9, 3), (8, 2), (12, 4)] if not quick else [(9, 3), (12, 4), (6, 2)]
     for P, Q in cases:
         for count in ((1, 7, 33, 80) if not quick else (33,)):
             for dtype in (F32, BF16, I32):

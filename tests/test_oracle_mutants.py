@@ -99,6 +99,13 @@ MUTANTS = {
     "ag_rank0_piece_only": ("(const char*)send[s] + i * es, es);", "(const char*)send[0] + i * es, es);"),
     "vector_of_4_elements": ("static size_t vec_elems(int dtype) { return 16 / elem_size(dtype); }",
                              "static size_t vec_elems(int dtype) { (void)dtype; return 4; }"),
+    "hier_chunks_by_group_count": ("    size_t L1 = round_up((count + (size_t)Q - 1) / (size_t)Q, V);",
+                                   "    size_t L1 = round_up((count + (size_t)G - 1) / (size_t)G, V);"),
+    "hier_subchunk_from_zero": ("    size_t c2 = (e - c1 * L1) / L2;", "    size_t c2 = (e / L2) % (size_t)G;"),
+    "tree_right_one_try": ("    for (int h = b / 2; h >= 1; h /= 2)\n        if (v + h <= P) return v + h;\n    return 0;",
+                           "    return v + b / 2 <= P ? v + b / 2 : 0;"),
+    "rne_ties_down": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;",
+                      "if (lower > 0x8000u) upper += 1;"),
     # 32-bit slips that only show at counts past 2^32 elements
     "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
     "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
