@@ -95,3 +95,32 @@ def test_edges_on_a_few_sms(P, dev):
                     check(comm, sends, count, dtype, algo, dev, want, f"TMA P={P} dtype={dtype} count={count} algo={algo}")
     finally:
         ar.ar_destroy(comm)
+
+
+def interleaved(P, Q, count, dtype):
+    """Group g's first rank holds the g-th of 2^24, 1, 1, -2^24 (0 from the
+    fifth group on); every other rank holds 0.  Each group's partial is then
+    that value, and the fold across groups shows its start group: the
+    hierarchical sub-chunk edges become visible."""
+    vals = [2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)]
+    sends = [np.zeros(count, dtype=np.float32) for _ in range(P)]
+    for g in range(min(4, P // Q)):
+        sends[g * Q][:] = vals[g]
+    if dtype == ar.AR_BFLOAT16:
+        sends = [pins.bf16_bits_torch(x) for x in sends]
+    return sends
+
+
+@pytest.mark.parametrize("P,Q", [(8, 2), (12, 3), (16, 4), (72, 8)])
+def test_hierarchical_subchunk_edges(P, Q, dev):
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, Q)
+        for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
+            for count in COUNTS:
+                sends = interleaved(P, Q, count, dtype)
+                want = oracle.allreduce_hier(sends, Q, dtype, oracle.SUM)
+                check(comm, sends, count, dtype, ar.AR_ALGO_HIER, dev, want,
+                      f"hier sub-chunks P={P} Q={Q} dtype={dtype} count={count}")
+    finally:
+        ar.ar_destroy(comm)
