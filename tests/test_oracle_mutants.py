@@ -106,6 +106,9 @@ MUTANTS = {
                            "    return v + b / 2 <= P ? v + b / 2 : 0;"),
     "rne_ties_down": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;",
                       "if (lower > 0x8000u) upper += 1;"),
+    "tree_halves_swapped": ("int t = e < oracle_tree_split(count, dtype) ? 0 : 1;",
+                            "int t = e < oracle_tree_split(count, dtype) ? 1 : 0;"),
+    "tree1_maps_like_tree0": ("return t == 0 ? v - 1 : v % P;", "return v - 1;"),
     # 32-bit slips that only show at counts past 2^32 elements
     "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
     "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
