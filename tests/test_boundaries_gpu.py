@@ -124,3 +124,31 @@ def test_hierarchical_subchunk_edges(P, Q, dev):
                       f"hier sub-chunks P={P} Q={Q} dtype={dtype} count={count}")
     finally:
         ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P", [4, 8, 12])
+def test_reduce_scatter_shard_edges(P, dev):
+    """Shard s is ring chunk s, folded from rank s: with the crafted data shard
+    0 reduces to 0 and shards 1..3 to 2, so a tile that crosses a shard edge
+    and keeps the wrong order shows.  Element-wise shards (not whole vectors),
+    whole-vector shards, and the TMA pipeline on 8 SMs (P <= 8)."""
+    comm = ar.ar_init(P)
+    try:
+        for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
+            for rc, blocks in ((5, 0), (1003, 0), (1024, 0), (65536 + 8, 0), (65536 + 8, 8), (3 * 4096 + 8, 8)):
+                if blocks and P > 8:
+                    continue
+                sends = crafted(P, P * rc, dtype)
+                want = oracle.reduce_scatter(sends, dtype, oracle.SUM, 1.0)
+                xs = [to_device(s, dtype, dev) for s in sends]
+                shards = [torch.empty(rc, dtype=xs[0].dtype, device=dev) for _ in range(P)]
+                ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, blocks)
+                ar.ar_reduce_scatter(comm, xs, shards, rc, dtype, ar.AR_SUM, 1.0)
+                torch.cuda.synchronize()
+                assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                for s in range(P):
+                    pins.assert_bitwise(to_host(shards[s]), want[s],
+                                        f"RS shard {s} P={P} dtype={dtype} rc={rc} blocks={blocks}")
+    finally:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 0)
+        ar.ar_destroy(comm)
