@@ -109,6 +109,10 @@ MUTANTS = {
     "tree_halves_swapped": ("int t = e < oracle_tree_split(count, dtype) ? 0 : 1;",
                             "int t = e < oracle_tree_split(count, dtype) ? 1 : 0;"),
     "tree1_maps_like_tree0": ("return t == 0 ? v - 1 : v % P;", "return v - 1;"),
+    "float_min_ties_take_later": ("else if (op == OR_MIN) acc.f = (x.f < acc.f) ? x.f : acc.f;",
+                                  "else if (op == OR_MIN) acc.f = (x.f <= acc.f) ? x.f : acc.f;"),
+    "float_max_ties_take_later": ("else acc.f = (x.f > acc.f) ? x.f : acc.f;",
+                                  "else acc.f = (x.f >= acc.f) ? x.f : acc.f;"),
     # 32-bit slips that only show at counts past 2^32 elements
     "chunk_index_32bit": ("int c = (int)(e / L);", "int c = (int)((uint32_t)e / L);"),
     "tree_split_32bit": ("size_t h = round_up((count + 1) / 2, vec_elems(dtype));",
