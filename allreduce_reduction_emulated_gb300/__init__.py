@@ -93,17 +93,31 @@ def library() -> ctypes.CDLL:
 _ESIZE = {AR_FLOAT32: 4, AR_BFLOAT16: 2, AR_INT32: 4}
 
 
-def _ptr(x, elems: int, dtype: int, what: str) -> int:
+def _current_device() -> int:
+    import torch
+
+    return torch.cuda.current_device()
+
+
+def _ptr(x, elems: int, dtype: int, what: str, device: int | None = None) -> int:
     """Device address of a buffer: a raw pointer (int) is passed through; a
-    tensor must be contiguous CUDA memory of at least `elems` elements of the
-    data type's size, else ArError(AR_ERR_INVALID_ARG) -- the library only sees
-    a pointer, so these are the checks it cannot make."""
+    tensor must be contiguous CUDA memory on the current device (`device`)
+    holding at least `elems` elements of the data type's size, else
+    ArError(AR_ERR_INVALID_ARG) -- the library only sees a pointer and launches
+    on the current device, so these are the checks it cannot make.  A tensor
+    on another GPU is refused before anything is launched: the kernels would
+    otherwise read or write that GPU's memory."""
     if isinstance(x, int):
         return x
     if not x.is_contiguous():
         raise ArError(AR_ERR_INVALID_ARG, f"{what}: tensor is not contiguous")
     if not x.is_cuda:
         raise ArError(AR_ERR_INVALID_ARG, f"{what}: tensor is not in CUDA memory")
+    if device is None:
+        device = _current_device()
+    if x.device.index != device:
+        raise ArError(AR_ERR_INVALID_ARG, f"{what}: tensor is on cuda:{x.device.index}, "
+                                          f"the current device is cuda:{device}")
     if x.element_size() != _ESIZE.get(int(dtype), 0):
         raise ArError(AR_ERR_INVALID_ARG, f"{what}: {x.element_size()}-byte elements for this data type")
     if x.numel() < elems:
@@ -112,7 +126,9 @@ def _ptr(x, elems: int, dtype: int, what: str) -> int:
 
 
 def _ptrs(bufs, elems: int, dtype: int, what: str):
-    return (ctypes.c_void_p * len(bufs))(*[_ptr(b, elems, dtype, f"{what}[{i}]") for i, b in enumerate(bufs)])
+    device = _current_device() if any(getattr(b, "is_cuda", False) for b in bufs) else None
+    return (ctypes.c_void_p * len(bufs))(*[_ptr(b, elems, dtype, f"{what}[{i}]", device)
+                                           for i, b in enumerate(bufs)])
 
 
 def _stream_handle(stream) -> int:
@@ -272,6 +288,9 @@ def allreduce(sends, recvs=None, op: str = "sum", algo: str = "auto", scale: flo
         if not t.is_cuda or not t.is_contiguous() or t.dtype != t0.dtype or t.numel() != t0.numel():
             raise ArError(AR_ERR_INVALID_ARG, "allreduce: tensors must be contiguous CUDA tensors "
                                               "of one dtype and size")
+        if t.device != t0.device:
+            raise ArError(AR_ERR_INVALID_ARG, f"allreduce: tensors on {t0.device} and {t.device}; "
+                                              "all must be on one GPU")
     key = (len(sends), t0.device.index if t0.device.index is not None else torch.cuda.current_device())
     with _comms_lock:
         if key not in _comms:

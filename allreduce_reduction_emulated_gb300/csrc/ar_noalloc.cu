@@ -16,6 +16,7 @@
 // out the kernel clears the staging words once.  The status word starts at
 // zero (module load) and is cleared whenever it is read.  Calls that overlap on the GPU (for example on two streams)
 // race on the array and must not be issued.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -39,20 +40,34 @@ static __device__ __align__(256) unsigned long long g_noalloc_scratch[kScratchWo
 namespace {
 
 struct DeviceState {
-  std::once_flag once;
-  cudaError_t setup = cudaSuccess;
+  std::mutex mu;
+  std::atomic<bool> ready{false};
   unsigned long long* base = nullptr;  // device address of g_noalloc_scratch
   int sms = 0;
 };
 
 DeviceState g_state[kMaxDevices];
 
-// Once per device, with that device current: the array's device address.
-// (In host code the symbol names a host-side stand-in, not device memory.)
-void set_up(DeviceState& s, int dev) {
-  s.setup = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.base), g_noalloc_scratch);
-  if (s.setup == cudaSuccess)
-    s.setup = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+// Per device, with that device current: the array's device address.  (In
+// host code the symbol names a host-side stand-in, not device memory.)  A
+// lookup that fails -- for example one attempted while the stream is being
+// captured -- leaves the device not ready, and the next call tries again.
+cudaError_t set_up(DeviceState& s, int dev) {
+  if (s.ready.load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.ready.load(std::memory_order_relaxed)) return cudaSuccess;
+  unsigned long long* base = nullptr;
+  int sms = 0;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&base), g_noalloc_scratch);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  s.base = base;
+  s.sms = sms;
+  s.ready.store(true, std::memory_order_release);
+  return cudaSuccess;
 }
 
 bool bad_overlap(const void* const* send, void* const* recv, int P, size_t bytes) {
@@ -88,8 +103,7 @@ extern "C" ar_status_t ar_allreduce_ll_noalloc(int nranks, const void* const* se
   }
   if (dev < 0 || dev >= kMaxDevices) return AR_ERR_UNSUPPORTED;
   DeviceState& s = g_state[dev];
-  std::call_once(s.once, set_up, std::ref(s), dev);
-  if (s.setup != cudaSuccess) return AR_ERR_CUDA;
+  if (set_up(s, dev) != cudaSuccess) return AR_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (count > 0) {

@@ -101,26 +101,35 @@ def test_binding_rejects_tensors_the_library_cannot_check():
         assert e.value.status == ar.AR_ERR_INVALID_ARG and reason in str(e.value)
 
 
+class CudaLike:
+    """Stands in for a CUDA tensor on device `index` (a CPU tensor's memory)."""
+
+    def __init__(self, t, index: int = 0):
+        import torch
+
+        self.t = t
+        self.is_cuda = True
+        self.device = torch.device("cuda", index)
+        self.dtype = t.dtype
+
+    def is_contiguous(self):
+        return self.t.is_contiguous()
+
+    def element_size(self):
+        return self.t.element_size()
+
+    def numel(self):
+        return self.t.numel()
+
+    def data_ptr(self):
+        return self.t.data_ptr()
+
+
 def test_binding_checks_length_and_element_size(monkeypatch):
     """Length and element size, with the CUDA check satisfied by a stand-in."""
     import torch
 
-    class CudaLike:
-        def __init__(self, t):
-            self.t = t
-            self.is_cuda = True
-
-        def is_contiguous(self):
-            return self.t.is_contiguous()
-
-        def element_size(self):
-            return self.t.element_size()
-
-        def numel(self):
-            return self.t.numel()
-
-        def data_ptr(self):
-            return self.t.data_ptr()
+    monkeypatch.setattr(ar, "_current_device", lambda: 0)
 
     short = CudaLike(torch.zeros(7))
     wide = CudaLike(torch.zeros(16, dtype=torch.float64))
@@ -152,3 +161,36 @@ def test_convenience_call_rejects_bad_names_and_empty_input():
     with pytest.raises(ar.ArError) as e:
         ar.allreduce([x, x])                       # CPU tensors: refused before the library
     assert "contiguous CUDA tensors" in str(e.value)
+
+
+def test_binding_refuses_a_tensor_on_another_gpu(monkeypatch):
+    """The kernels launch on the current device; a buffer on another GPU is
+    refused with AR_ERR_INVALID_ARG before the library is called."""
+    import torch
+
+    monkeypatch.setattr(ar, "_current_device", lambda: 0)
+
+    def fail(*a, **k):
+        raise AssertionError("the library must not be called")
+
+    monkeypatch.setattr(ar, "library", lambda: type("L", (), {"__getattr__": lambda self, n: fail,
+                                                             "ar_get_error_string": lambda self, s: b"x"})())
+    here = [CudaLike(torch.zeros(16)) for _ in range(2)]
+    there = CudaLike(torch.zeros(16), index=1)
+    calls = (
+        lambda: ar.ar_allreduce(1, [here[0], there], here, 16, ar.AR_FLOAT32),
+        lambda: ar.ar_allreduce(1, here, [here[0], there], 16, ar.AR_FLOAT32),
+        lambda: ar.ar_reduce_scatter(1, [CudaLike(torch.zeros(32)), CudaLike(torch.zeros(32), 1)],
+                                     here, 16, ar.AR_FLOAT32),
+        lambda: ar.ar_all_gather(1, here, [CudaLike(torch.zeros(32), 1), CudaLike(torch.zeros(32))],
+                                 16, ar.AR_FLOAT32),
+        lambda: ar.ar_allreduce_ll_noalloc([there, here[1]], here, 16, ar.AR_FLOAT32),
+    )
+    for call in calls:
+        with pytest.raises(ar.ArError) as e:
+            call()
+        assert e.value.status == ar.AR_ERR_INVALID_ARG and "cuda:1" in str(e.value)
+    # the convenience call: every tensor on the first tensor's device
+    with pytest.raises(ar.ArError) as e:
+        ar.allreduce([here[0], there])
+    assert e.value.status == ar.AR_ERR_INVALID_ARG and "one GPU" in str(e.value)

@@ -4,21 +4,25 @@ Some callers of this library cannot allocate device memory: their device
 memory belongs to a framework's pool, they run in a latency-critical loop
 where cudaMalloc / cudaFree may synchronize the device, or they may not
 allocate after start-up.  ar_allreduce_ll_noalloc serves them from one
-fixed array compiled into the library.  This test calls it through the C ABI
-twice in a row and checks each result against the communicator-based
-ar_allreduce (LL) on the same inputs, bit for bit -- the tolerance of every
-fp32 test here -- then checks that requests beyond the array's limits are
-rejected.  It lives in its own file, collected last, and passes alone in a
-fresh process as well as after the other tests (the array keeps the last
-call's contents; each call must still give its own result).
+fixed array compiled into the library.  These tests call it through the C
+ABI and check its results against the CPU oracle in the ring order (which
+the LL protocol follows) for 1, 3 and 8 ranks, every data type and op, and
+counts from one element to the array's 64 KiB limit, and, twice in a row,
+against the communicator-based ar_allreduce (LL) on the same inputs -- bit
+for bit, the tolerance of every fp32 test here.  They then check that
+requests beyond the array's limits are rejected.  The file is collected last
+and passes alone in a fresh process as well as after the other tests (the
+array keeps the last call's contents; each call must still give its own
+result).
 """
 import numpy as np
 import pytest
 import torch
 
 import allreduce_reduction_emulated_gb300 as ar
+import oracle
 import pins
-from gpu_util import to_device, to_host
+from gpu_util import Guarded, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +36,34 @@ def dev():
     __graft_entry__.build()
     torch.cuda.set_device(0)
     return torch.device("cuda:0")
+
+
+# (dtype, op, scale): fp32 sum with the DDP mean, bf16 sum (odd counts end in a
+# 2-byte half of the last staged word), int32 min and max
+CASES = [(ar.AR_FLOAT32, ar.AR_SUM, 0.125), (ar.AR_BFLOAT16, ar.AR_SUM, 1.0),
+         (ar.AR_INT32, ar.AR_MIN, 1.0), (ar.AR_INT32, ar.AR_MAX, 1.0)]
+
+
+@pytest.mark.parametrize("P", [1, 3, 8])
+def test_matches_the_oracle(P, dev):
+    """Every element of every rank against the oracle's ring order; fewer
+    ranks than the array's 8 slots, counts 1 and 7 and the 64 KiB maximum."""
+    rng = np.random.default_rng(500 + P)
+    for dtype, op, scale in CASES:
+        esize = 2 if dtype == ar.AR_BFLOAT16 else 4
+        for count in (1, 7, ar.AR_NOALLOC_MAX_BYTES // esize - (1 if dtype == ar.AR_BFLOAT16 else 0),
+                      ar.AR_NOALLOC_MAX_BYTES // esize):
+            sends_np = pins.random_inputs(rng, P, count, dtype)
+            sends = [to_device(a, dtype, dev) for a in sends_np]
+            outs = [Guarded(count, dtype, dev) for _ in range(P)]
+            status = ar.ar_allreduce_ll_noalloc(sends, [o.tensor for o in outs], count, dtype, op,
+                                                scale, wait_status=True)
+            assert status == ar.AR_SUCCESS
+            want = oracle.allreduce(sends_np, dtype, op, oracle.RING, scale)
+            for r in range(P):
+                assert outs[r].guards_intact(), f"write outside rank {r}'s receive buffer"
+                pins.assert_bitwise(to_host(outs[r].tensor), want[r],
+                                    f"P={P} dtype={dtype} op={op} count={count} rank={r}")
 
 
 def test_two_calls_match_the_communicator_entry_point(dev):
