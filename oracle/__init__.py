@@ -139,8 +139,9 @@ class Oracle:
         return out
 
     def allreduce_hier(self, sends, group: int, dtype: int, op: int = SUM, scale: float = 1.0,
-                       begin: int = 0, end: int | None = None):
-        """Hierarchical all-reduce, groups of `group` consecutive ranks."""
+                       begin: int = 0, end: int | None = None, recvs=None):
+        """Hierarchical all-reduce, groups of `group` consecutive ranks (output
+        elements [begin, end) only, as for allreduce)."""
         P = len(sends)
         count = int(sends[0].shape[0])
         want = NP_DTYPE[dtype]
@@ -148,7 +149,8 @@ class Oracle:
         for s in sends:
             if s.dtype != want or s.shape != (count,):
                 raise OracleError("all send arrays must share dtype and length")
-        recvs = [np.zeros(count, dtype=want) for _ in range(P)]
+        if recvs is None:
+            recvs = [np.zeros(count, dtype=want) for _ in range(P)]
         end = count if end is None else end
         sp = (ctypes.c_void_p * P)(*[s.ctypes.data for s in sends])
         rp = (ctypes.c_void_p * P)(*[r.ctypes.data for r in recvs])

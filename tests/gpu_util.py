@@ -1,6 +1,9 @@
 """Helpers for the GPU parity tests (inputs, sampling, comparisons)."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -106,3 +109,69 @@ def all_ranks_identical(recvs) -> bool:
         if not torch.equal(a, b):
             return False
     return True
+
+
+# ------------------------------------------------------ whole-array parity
+
+ORACLE_THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def oracle_full(host_sends, dtype: int, op: int, algo: int, scale: float = 1.0,
+                group: int | None = None) -> np.ndarray:
+    """The oracle's all-reduce result for every element (one array: every
+    rank receives the same).  The elements are cut into ranges that run as
+    separate single-threaded oracle calls on a thread pool (ctypes releases
+    the GIL); each call folds its elements in the order the full count
+    defines, so the ranges change nothing but the wall time.  group: the
+    hierarchical order with groups of that many ranks."""
+    P, count = len(host_sends), int(host_sends[0].shape[0])
+    out = np.empty(count, dtype=oracle.NP_DTYPE[dtype])
+    if count == 0:
+        return out
+    step = max(1 << 16, -(-count // (4 * ORACLE_THREADS)))
+    ranges = [(b, min(count, b + step)) for b in range(0, count, step)]
+    outs = [out] * P
+
+    def run(be):
+        b, e = be
+        if group is not None:
+            oracle.allreduce_hier(host_sends, group, dtype, op, scale, b, e, recvs=outs)
+        else:
+            oracle.allreduce(host_sends, dtype, op, algo, scale, b, e, recvs=outs)
+
+    if len(ranges) == 1:
+        run(ranges[0])
+    else:
+        with ThreadPoolExecutor(ORACLE_THREADS) as ex:
+            list(ex.map(run, ranges))
+    return out
+
+
+def assert_equal_every_element(got, want: np.ndarray, what: str):
+    """A device (or host) result against the oracle's, bit for bit, over the
+    whole array; names the first differing indices."""
+    g = to_host(got) if isinstance(got, torch.Tensor) else got
+    if g.shape != want.shape:
+        raise AssertionError(f"{what}: shape {g.shape} vs {want.shape}")
+    bits = {2: np.uint16, 4: np.uint32}[want.dtype.itemsize]
+    gi, wi = np.ascontiguousarray(g).view(bits), want.view(bits)
+    if np.array_equal(gi, wi):
+        return
+    bad = np.nonzero(gi != wi)[0]
+    raise AssertionError(f"{what}: {bad.size} of {want.size} elements differ, first at "
+                         f"{bad[:5].tolist()}: {g[bad[:5]]} vs {want[bad[:5]]}")
+
+
+def host_inputs(sends, kind: str, seed: int, sigma: float = 1.0, start: int = 0,
+                n_check: int = 256) -> list:
+    """Host copies of the device inputs, checked against the host generator
+    at sampled indices (the oracle's inputs are the generator's values)."""
+    host = [to_host(s) for s in sends]
+    count = int(host[0].shape[0])
+    rng = np.random.default_rng(seed + 7)
+    idx = np.unique(np.concatenate([rng.integers(0, count, size=min(n_check, count)), [0, count - 1]]))
+    cols = host_columns(kind, seed, len(host), idx, sigma, start)
+    for r, h in enumerate(host):
+        if not np.array_equal(h[idx].view(np.uint8), cols[r].view(np.uint8)):
+            raise AssertionError(f"rank {r}: device inputs differ from the host generator")
+    return host

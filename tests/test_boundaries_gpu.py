@@ -1,12 +1,16 @@
 """Ring-chunk edges and the tree split on the GPU, made visible by the data.
 
-Ranks 0..3 hold 2^24, 1, 1, -2^24 (exact in fp32 and bf16) and every other
-rank holds 0.  A fold that meets rank 0's 2^24 before the two 1s absorbs them
-and ends at 0; any other order ends at 2.  So each output element shows which
-order folded it, and a chunk edge or tree split off by even one 16-byte vector
-changes whole elements -- which random data, whose fp32 sums are mostly
-exact, rarely shows.  Every element is compared with the oracle, whose own
-edges are pinned by hand-worked boundaries.  The ring chunks and the split
+Ranks c, c+1, c+2, c+3 (mod P) hold 2^24, 1, 1, -2^24 (exact in fp32 and
+bf16) and every other rank holds 0.  A fold that meets 2^24 before the two 1s
+absorbs them and ends at 0; a fold that meets a 1 first ends at 2.  In the
+ring order chunk k starts at rank k, so chunks c+1, c+2 and c+3 reduce to 2
+and every other chunk to 0: the edges c|c+1 and c+3|c+4 are 0|2 steps.  The
+pattern runs from every start rank c, so every chunk edge (and every
+reduce-scatter shard edge) is such a step at least once, and an edge off by
+even one 16-byte vector changes whole elements -- which random data, whose
+fp32 sums are mostly exact, rarely shows.  Every element is compared with the
+oracle, whose own edges are pinned by hand-worked boundaries.  The ring
+chunks and the split
 follow "NCCL, NIXL, and Distributed GPU Communication" (section
 "Reduce-scatter") and "NCCL and NVSHMEM -- two GPU communication models,
 side by side" (the double binary tree).
@@ -18,7 +22,7 @@ import torch
 import allreduce_reduction_emulated_gb300 as ar
 import oracle
 import pins
-from gpu_util import to_device, to_host
+from gpu_util import oracle_full, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -36,8 +40,10 @@ def dev():
     return torch.device("cuda:0")
 
 
-def crafted(P, count, dtype):
-    vals = [2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)] + [0.0] * (P - 4)
+def crafted(P, count, dtype, c=0):
+    """2^24, 1, 1, -2^24 on ranks c .. c+3 (mod P), 0 elsewhere."""
+    base = [2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)] + [0.0] * (P - 4)
+    vals = [base[(r - c) % P] for r in range(P)]
     sends = [np.full(count, v, dtype=np.float32) for v in vals]
     if dtype == ar.AR_BFLOAT16:
         sends = [pins.bf16_bits_torch(x) for x in sends]
@@ -52,7 +58,16 @@ def check(comm, sends, count, dtype, algo, dev, want, tag):
     torch.cuda.synchronize()
     assert ar.ar_get_status(comm) == ar.AR_SUCCESS
     for r in (0, P - 1):
-        pins.assert_bitwise(to_host(outs[r]), want[r], f"{tag} rank {r}")
+        w = want if isinstance(want, np.ndarray) else want[r]
+        pins.assert_bitwise(to_host(outs[r]), w, f"{tag} rank {r}")
+
+
+def start_ranks(P, count=None):
+    """Every start rank; at 72 ranks only for the two counts whose chunks span
+    several vectors (the others leave most chunks empty or one vector long)."""
+    if P > 12 and count is not None and count < 4096:
+        return [0]
+    return list(range(P))
 
 
 @pytest.mark.parametrize("P,Q", [(4, 2), (5, 0), (8, 4), (12, 4), (72, 8)])
@@ -64,18 +79,20 @@ def test_edges_every_algorithm(P, Q, dev):
         for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
             esize = 2 if dtype == ar.AR_BFLOAT16 else 4
             for count in COUNTS:
-                sends = crafted(P, count, dtype)
-                ring = oracle.allreduce(sends, dtype, oracle.SUM, oracle.RING)
-                tree = oracle.allreduce(sends, dtype, oracle.SUM, oracle.TREE)
-                algos = [(ar.AR_ALGO_RING, ring), (ar.AR_ALGO_TREE, tree)]
-                if count * esize <= 65536:
-                    algos.append((ar.AR_ALGO_LL, ring))
-                if count * esize <= 1 << 20:
-                    algos.append((ar.AR_ALGO_LL128, ring))
-                if Q:
-                    algos.append((ar.AR_ALGO_HIER, oracle.allreduce_hier(sends, Q, dtype, oracle.SUM)))
-                for algo, want in algos:
-                    check(comm, sends, count, dtype, algo, dev, want, f"P={P} dtype={dtype} count={count} algo={algo}")
+                for c in start_ranks(P, count):
+                    sends = crafted(P, count, dtype, c)
+                    ring = oracle_full(sends, dtype, oracle.SUM, oracle.RING)
+                    tree = oracle_full(sends, dtype, oracle.SUM, oracle.TREE)
+                    algos = [(ar.AR_ALGO_RING, ring), (ar.AR_ALGO_TREE, tree)]
+                    if count * esize <= 65536:
+                        algos.append((ar.AR_ALGO_LL, ring))
+                    if count * esize <= 1 << 20:
+                        algos.append((ar.AR_ALGO_LL128, ring))
+                    if Q:
+                        algos.append((ar.AR_ALGO_HIER, oracle_full(sends, dtype, oracle.SUM, None, group=Q)))
+                    for algo, want in algos:
+                        check(comm, sends, count, dtype, algo, dev, want,
+                              f"P={P} c={c} dtype={dtype} count={count} algo={algo}")
     finally:
         ar.ar_destroy(comm)
 
@@ -89,10 +106,14 @@ def test_edges_on_a_few_sms(P, dev):
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 8)
         for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
             for count in (65536 + 13, (1 << 20) + 5, 3 * (1 << 20) + 1000):
-                sends = crafted(P, count, dtype)
-                for algo, oalgo in ((ar.AR_ALGO_RING, oracle.RING), (ar.AR_ALGO_TREE, oracle.TREE)):
-                    want = oracle.allreduce(sends, dtype, oracle.SUM, oalgo)
-                    check(comm, sends, count, dtype, algo, dev, want, f"TMA P={P} dtype={dtype} count={count} algo={algo}")
+                for c in start_ranks(P):
+                    sends = crafted(P, count, dtype, c)
+                    for algo, oalgo in ((ar.AR_ALGO_RING, oracle.RING), (ar.AR_ALGO_TREE, oracle.TREE)):
+                        if algo == ar.AR_ALGO_TREE and c % 2:
+                            continue                       # the split: every other start rank suffices
+                        want = oracle_full(sends, dtype, oracle.SUM, oalgo)
+                        check(comm, sends, count, dtype, algo, dev, want,
+                              f"TMA P={P} c={c} dtype={dtype} count={count} algo={algo}")
     finally:
         ar.ar_destroy(comm)
 
@@ -128,27 +149,30 @@ def test_hierarchical_subchunk_edges(P, Q, dev):
 
 @pytest.mark.parametrize("P", [4, 8, 12])
 def test_reduce_scatter_shard_edges(P, dev):
-    """Shard s is ring chunk s, folded from rank s: with the crafted data shard
-    0 reduces to 0 and shards 1..3 to 2, so a tile that crosses a shard edge
-    and keeps the wrong order shows.  Element-wise shards (not whole vectors),
-    whole-vector shards, and the TMA pipeline on 8 SMs (P <= 8)."""
+    """Shard s is ring chunk s, folded from rank s: with the crafted data
+    started at rank c, shards c+1..c+3 reduce to 2 and the others to 0, so a
+    tile that crosses a shard edge and keeps the wrong order shows; every start
+    rank runs, so every shard edge is a 0|2 step once.  Element-wise shards
+    (not whole vectors), whole-vector shards, and the TMA pipeline on 8 SMs
+    (P <= 8)."""
     comm = ar.ar_init(P)
     try:
         for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
             for rc, blocks in ((5, 0), (1003, 0), (1024, 0), (65536 + 8, 0), (65536 + 8, 8), (3 * 4096 + 8, 8)):
                 if blocks and P > 8:
                     continue
-                sends = crafted(P, P * rc, dtype)
-                want = oracle.reduce_scatter(sends, dtype, oracle.SUM, 1.0)
-                xs = [to_device(s, dtype, dev) for s in sends]
-                shards = [torch.empty(rc, dtype=xs[0].dtype, device=dev) for _ in range(P)]
-                ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, blocks)
-                ar.ar_reduce_scatter(comm, xs, shards, rc, dtype, ar.AR_SUM, 1.0)
-                torch.cuda.synchronize()
-                assert ar.ar_get_status(comm) == ar.AR_SUCCESS
-                for s in range(P):
-                    pins.assert_bitwise(to_host(shards[s]), want[s],
-                                        f"RS shard {s} P={P} dtype={dtype} rc={rc} blocks={blocks}")
+                for c in start_ranks(P):
+                    sends = crafted(P, P * rc, dtype, c)
+                    want = oracle.reduce_scatter(sends, dtype, oracle.SUM, 1.0)
+                    xs = [to_device(s, dtype, dev) for s in sends]
+                    shards = [torch.empty(rc, dtype=xs[0].dtype, device=dev) for _ in range(P)]
+                    ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, blocks)
+                    ar.ar_reduce_scatter(comm, xs, shards, rc, dtype, ar.AR_SUM, 1.0)
+                    torch.cuda.synchronize()
+                    assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                    for s in range(P):
+                        pins.assert_bitwise(to_host(shards[s]), want[s],
+                                            f"RS shard {s} P={P} c={c} dtype={dtype} rc={rc} blocks={blocks}")
     finally:
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 0)
         ar.ar_destroy(comm)

@@ -13,7 +13,8 @@ import torch
 import allreduce_reduction_emulated_gb300 as ar
 import oracle
 import pins
-from gpu_util import VEC, Guarded, all_ranks_identical, device_inputs, to_device, to_host
+from gpu_util import (VEC, Guarded, all_ranks_identical, assert_equal_every_element, device_inputs, host_inputs,
+                      to_device, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -141,8 +142,8 @@ def test_layout_errors(dev, comms):
 
 def test_reduce_scatter_then_all_gather_is_the_ring_allreduce(dev, comms):
     """P=8, 2,097,152 fp32 per shard (64 MiB per rank), scale 1/8: RS + AG on
-    the GPU equals the GPU ring all-reduce for every element, and sampled RS
-    outputs equal the oracle."""
+    the GPU equals the GPU ring all-reduce for every element, and every
+    reduce-scatter output element equals the oracle's."""
     P, rc, sigma = 8, 2 * 1024 * 1024, 1e-3
     comm = comms(P)
     sends = device_inputs("normal", 0, P, P * rc, dev, sigma)
@@ -156,10 +157,8 @@ def test_reduce_scatter_then_all_gather_is_the_ring_allreduce(dev, comms):
     for r in range(P):
         assert torch.equal(gathered[r].view(torch.int32), ref[r].view(torch.int32)), f"rank {r}"
     assert all_ranks_identical(gathered)
-    rng = np.random.default_rng(5)
-    idx = np.unique(np.concatenate([rng.integers(0, P * rc, 512), [0, rc - 1, rc, P * rc - 1]]))
-    it = torch.from_numpy(idx).to(dev)
-    cols = np.stack([to_host(s.index_select(0, it)) for s in sends])
-    want = oracle.allreduce_sampled(cols, idx, P * rc, ar.AR_FLOAT32, oracle.SUM, oracle.RING, 0.125)
-    got = np.array([to_host(shards[i // rc][i % rc:i % rc + 1])[0] for i in idx], dtype=np.float32)
-    pins.assert_bitwise(got, want, "sampled reduce-scatter outputs")
+    host = host_inputs(sends, "normal", 0, sigma)
+    want = oracle.reduce_scatter(host, ar.AR_FLOAT32, oracle.SUM, 0.125)
+    for s in range(P):
+        assert_equal_every_element(shards[s], want[s], f"reduce-scatter shard {s}")
+    assert_equal_every_element(gathered[0], np.concatenate(want), "all-gather of the shards, rank 0")

@@ -11,7 +11,8 @@ import torch
 import allreduce_reduction_emulated_gb300 as ar
 import oracle
 import pins
-from gpu_util import Guarded, all_ranks_identical, device_inputs, host_columns, sample_indices, to_device, to_host
+from gpu_util import (Guarded, all_ranks_identical, assert_equal_every_element, device_inputs, host_inputs,
+                      oracle_full, to_device, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,8 +56,8 @@ def test_hier_small(P, Q, dev):
 
 
 def test_hier_full_size_p72(dev):
-    """P=72 in 9 groups of 8, 4,194,304 elements per rank (16 MiB): fp32 sampled
-    against the oracle; int32 exact, and equal to the ring (integers)."""
+    """P=72 in 9 groups of 8, 4,194,304 elements per rank (16 MiB): fp32 every
+    element against the oracle; int32 exact, and equal to the ring (integers)."""
     P, Q, count = 72, 8, 4 * 1024 * 1024
     comm = ar.ar_init(P)
     try:
@@ -65,12 +66,9 @@ def test_hier_full_size_p72(dev):
         recvs = [torch.empty_like(s) for s in sends]
         ar.ar_allreduce(comm, sends, recvs, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_HIER, 1.0 / 72)
         torch.cuda.synchronize()
-        idx = sample_indices(count, Q, ar.AR_FLOAT32, n_random=2048, seed=4)
-        cols = host_columns("normal", 3, P, idx, 1e-3)
-        want = oracle.allreduce_hier_sampled(cols, idx, count, Q, ar.AR_FLOAT32, oracle.SUM, 1.0 / 72)
-        it = torch.from_numpy(idx).to(dev)
-        for r in (0, 35, 71):
-            pins.assert_bitwise(to_host(recvs[r].index_select(0, it)), want, f"P=72 hier fp32 rank {r}")
+        host = host_inputs(sends, "normal", 3, 1e-3)
+        want = oracle_full(host, ar.AR_FLOAT32, oracle.SUM, None, 1.0 / 72, group=Q)
+        assert_equal_every_element(recvs[0], want, "P=72 hier fp32 rank 0")
         assert all_ranks_identical(recvs)
         del sends, recvs
         ints = device_inputs("int", 0, P, count, dev)

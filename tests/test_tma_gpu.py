@@ -16,7 +16,8 @@ import torch
 import allreduce_reduction_emulated_gb300 as ar
 import oracle
 import pins
-from gpu_util import VEC, Guarded, device_inputs, to_device, to_host
+from gpu_util import (VEC, Guarded, assert_equal_every_element, device_inputs, host_inputs, oracle_full,
+                      to_device, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -70,8 +71,9 @@ def test_capped_calls_match_the_oracle(P, dtype, dev, capfd):
 
 
 def test_full_size_equals_the_uncapped_kernel(dev):
-    """8 x 64 MiB fp32, ring, scale 1/8 on 64 SMs: element for element the
-    uncapped kernel's result, in place and out of place."""
+    """8 x 64 MiB fp32, ring, scale 1/8 on 64 SMs: every element against the
+    oracle, and element for element the uncapped kernel's result, in place
+    and out of place."""
     P, count = 8, 16 * 1024 * 1024
     comm = ar.ar_init(P)
     try:
@@ -82,6 +84,8 @@ def test_full_size_equals_the_uncapped_kernel(dev):
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 64)
         ar.ar_allreduce(comm, sends, got, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125)
         torch.cuda.synchronize()
+        want = oracle_full(host_inputs(sends, "normal", 0, 1e-3), ar.AR_FLOAT32, oracle.SUM, oracle.RING, 0.125)
+        assert_equal_every_element(got[0], want, "64 SMs rank 0")
         for r in range(P):
             assert torch.equal(got[r].view(torch.int32), ref[r].view(torch.int32)), f"rank {r}"
         inplace = [s.clone() for s in sends]
@@ -279,8 +283,8 @@ def test_first_capped_call_inside_a_graph_capture(dev):
 
 def test_full_size_reduce_scatter_and_all_gather_on_64_sms(dev):
     """P=8, 8 MiB shards / pieces (the bench's sizes): the capped TMA kernels
-    equal the uncapped kernels element for element, and sampled reduce-scatter
-    outputs equal the oracle."""
+    equal the uncapped kernels element for element, and every reduce-scatter
+    output element equals the oracle's."""
     P, rc = 8, 2 * 1024 * 1024
     comm = ar.ar_init(P)
     try:
@@ -300,12 +304,9 @@ def test_full_size_reduce_scatter_and_all_gather_on_64_sms(dev):
         for r in range(P):
             assert torch.equal(got[r].view(torch.int32), ref[r].view(torch.int32)), f"RS rank {r}"
             assert torch.equal(gathered[r].view(torch.int32), gathered_ref[r].view(torch.int32)), f"AG rank {r}"
-        rng = np.random.default_rng(6)
-        idx = np.unique(np.concatenate([rng.integers(0, P * rc, 512), [0, rc - 1, rc, P * rc - 1]]))
-        it = torch.from_numpy(idx).to(dev)
-        cols = np.stack([to_host(s.index_select(0, it)) for s in sends])
-        want = oracle.allreduce_sampled(cols, idx, P * rc, ar.AR_FLOAT32, oracle.SUM, oracle.RING, 0.125)
-        flat = torch.cat(got)
-        pins.assert_bitwise(to_host(flat.index_select(0, it)), want, "sampled capped reduce-scatter outputs")
+        want = oracle.reduce_scatter(host_inputs(sends, "normal", 0, 1e-3), ar.AR_FLOAT32, oracle.SUM, 0.125)
+        for s in range(P):
+            assert_equal_every_element(got[s], want[s], f"capped reduce-scatter shard {s}")
+        assert_equal_every_element(gathered[0], np.concatenate(want), "all-gather of the shards, rank 0")
     finally:
         ar.ar_destroy(comm)
