@@ -44,7 +44,40 @@ TREE_EXPRESSIONS = {
     6: ("((x3+((x1+x0)+x2))+(x5+x4))", "((x4+((x2+x1)+x3))+(x0+x5))"),
     7: ("((x3+((x1+x0)+x2))+((x5+x4)+x6))", "((x4+((x2+x1)+x3))+((x6+x5)+x0))"),
     8: ("(x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))", "(x0+((x4+((x2+x1)+x3))+((x6+x5)+x7)))"),
+    # Above 8 the root is still label 8 and its left subtree is labels 1..7 as
+    # for P = 8; what changes is the right spine, which P truncates:
+    #   P = 9:  root 8 tries 8+4 = 12 and 8+2 = 10, both past 9, and takes 8+1 = 9,
+    #           a leaf (two levels skipped at one node);
+    #   P = 10: root 8 skips 12 and takes 10; label 10 (lowbit 2) has left 9 and no
+    #           right child (11 > 10);
+    #   P = 11: as 10, and label 10 gets the right child 11;
+    #   P = 12: root 8 takes 12 (lowbit 4): left 10 (children 9, 11), and no right
+    #           child (14 and 13 are past 12);
+    #   P = 13: as 12, but label 12 skips 14 and takes 13.
+    # Tree 0 writes label v as rank v - 1; tree 1 as rank v mod P, so the largest
+    # label P becomes rank 0.
+    9: ("((x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))+x8)",
+        "((x8+((x4+((x2+x1)+x3))+((x6+x5)+x7)))+x0)"),
+    10: ("((x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))+(x9+x8))",
+         "((x8+((x4+((x2+x1)+x3))+((x6+x5)+x7)))+(x0+x9))"),
+    11: ("((x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))+((x9+x8)+x10))",
+         "((x8+((x4+((x2+x1)+x3))+((x6+x5)+x7)))+((x10+x9)+x0))"),
+    12: ("((x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))+(x11+((x9+x8)+x10)))",
+         "((x8+((x4+((x2+x1)+x3))+((x6+x5)+x7)))+(x0+((x10+x9)+x11)))"),
+    13: ("((x7+((x3+((x1+x0)+x2))+((x5+x4)+x6)))+((x11+((x9+x8)+x10))+x12))",
+         "((x8+((x4+((x2+x1)+x3))+((x6+x5)+x7)))+((x12+((x10+x9)+x11))+x0))"),
 }
+
+# P = 72, worked by hand: the root is label 64; its right child search skips
+# 64+32 = 96 and 64+16 = 80 and takes 64+8 = 72.  Label 72 (lowbit 8) has the
+# left child 68 and no right child (76, 74, 73 are past 72); 68 (lowbit 4) has
+# children 66 and 70, which have the leaves 65, 67 and 69, 71.  The root's left
+# child is label 32, the complete subtree of labels 1..63 -- the same subtree
+# as the root's left child at P = 64.  So the expression is
+# ((own(64) + S) + R) with S the P = 64 tree's left subtree and R below.
+TREE72_RIGHT = ("(x71+((x67+((x65+x64)+x66))+((x69+x68)+x70)))",   # tree 0: label v -> rank v - 1
+                "(x0+((x68+((x66+x65)+x67))+((x70+x69)+x71)))")    # tree 1: label 72 -> rank 0
+TREE72_ROOT = ("x63", "x64")
 
 VEC = {F32: 4, BF16: 8, I32: 4}   # elements per 16-byte vector
 
@@ -314,6 +347,20 @@ def pin_tree_expressions(O):
                     want.append(eval_expr(expr, [x[e] for x in xs], dtype, SUM))
                 assert_bitwise(outs[0], narrow(want, dtype, 1.0),
                                f"tree numeric P={P} dtype={dtype} count={count}")
+
+
+def pin_tree72_spine(O):
+    """The P = 72 trees against the hand-worked right spine above: the root's
+    own rank, its left subtree (that of P = 64, whose root is label 64 too),
+    then the truncated right subtree under label 72."""
+    for t in (0, 1):
+        e64 = O.tree_expr(64, t)
+        root64 = "x63" if t == 0 else "x0"                 # label 64: rank 63 / rank 64 mod 64
+        assert e64.startswith(f"({root64}+") and e64.endswith(")"), e64[:40]
+        left = e64[len(root64) + 2:-1]
+        want = f"(({TREE72_ROOT[t]}+{left})+{TREE72_RIGHT[t]})"
+        got = O.tree_expr(72, t)
+        assert got == want, f"P=72 tree {t}: ...{got[-90:]} != ...{want[-90:]}"
 
 
 def pin_tree_structure(O):
@@ -807,7 +854,7 @@ def pin_hierarchical_order_independent(O):
 
 
 ALL_PINS = [pin_worked_example, pin_outputs_identical, pin_ring_simulation, pin_tree_expressions,
-            pin_tree_structure, pin_tree_definition, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
+            pin_tree72_spine, pin_tree_structure, pin_tree_definition, pin_signed_zero_ties, pin_order_independent, pin_error_bound, pin_scale, pin_bf16_rne,
             pin_sampled_matches_full, pin_reduce_scatter_worked_example, pin_all_gather_worked_example,
             pin_allreduce_is_reduce_scatter_then_all_gather, pin_reduce_scatter_ring_steps,
             pin_collectives_order_independent, pin_hierarchical_steps,

@@ -104,6 +104,8 @@ MUTANTS = {
     "hier_subchunk_from_zero": ("    size_t c2 = (e - c1 * L1) / L2;", "    size_t c2 = (e / L2) % (size_t)G;"),
     "tree_right_one_try": ("    for (int h = b / 2; h >= 1; h /= 2)\n        if (v + h <= P) return v + h;\n    return 0;",
                            "    return v + b / 2 <= P ? v + b / 2 : 0;"),
+    "tree_right_two_tries": ("    for (int h = b / 2; h >= 1; h /= 2)\n        if (v + h <= P) return v + h;\n    return 0;",
+                             "    for (int h = b / 2; h >= 1 && h >= b / 4; h /= 2)\n        if (v + h <= P) return v + h;\n    return 0;"),
     "rne_ties_down": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;",
                       "if (lower > 0x8000u) upper += 1;"),
     "tree_halves_swapped": ("int t = e < oracle_tree_split(count, dtype) ? 0 : 1;",
