@@ -154,18 +154,31 @@ ar_status_t ar_allreduce(ar_comm_t comm, const void* const* sendbufs, void* cons
 /*
  * Device-side status of the calls made so far on `comm`: AR_SUCCESS or
  * AR_ERR_TIMEOUT (an LL / LL128 flag wait or a TMA-kernel mbarrier wait gave
- * up; that call's output is incomplete).
+ * up; that call's output is incomplete).  The collective runs asynchronously
+ * on the caller's stream and is complete only after a stream synchronize
+ * ("NCCL and NVSHMEM -- two GPU communication models, side by side", the
+ * host-code example), so an error found while it runs can only be read
+ * afterwards; reporting a wait that ran out instead of hanging follows the
+ * fail-fast default and the timeout advice of the lecture_068 page, section 08
+ * (debug and stability).
  * Reads and clears the device status word with a synchronous copy, so call it
  * after synchronizing the streams the calls ran on.  AR_ERR_CUDA if the copy
  * fails, AR_ERR_INVALID_ARG for a NULL comm.
  */
 ar_status_t ar_get_status(ar_comm_t comm);
 
-/* Static, human-readable name of a status code (never NULL). */
+/* Static, human-readable name of a status code (never NULL).  The pages have
+ * no counterpart: it exists so that callers and the AR_DEBUG trace can log a
+ * status by name, the observability that the lecture_068 page, section 08,
+ * asks of a communication library (NCCL_DEBUG=INFO as the first tool). */
 const char* ar_get_error_string(ar_status_t status);
 
 /* Frees the communicator's device memory.  Synchronizes the device first.
- * NULL is accepted (no-op). */
+ * NULL is accepted (no-op).  The pages' host-code example creates the
+ * communicator once (ncclCommInitRank) and never shows its teardown; the
+ * checklist of "NCCL, NIXL, and Distributed GPU Communication" says a
+ * communicator is set up once and reused, never created and destroyed inside
+ * the training loop -- so this call belongs at shutdown. */
 ar_status_t ar_destroy(ar_comm_t comm);
 
 /*
