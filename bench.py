@@ -59,6 +59,8 @@ PROFILES = {
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
 
+HEADLINE = "p8_64MiB_fp32_ring_ddp_mean"
+
 WORKLOADS = {
     # the headline: 8 ranks x 64 MiB fp32, ring order, DDP mean
     "p8_64MiB_fp32_ring_ddp_mean": dict(P=8, count=16 * 1024 * 1024, kind="normal", sigma=1e-3,
@@ -139,7 +141,7 @@ def parse_args():
                     help="timed steps (default: 6000; 200 with --ddp-buckets, 30 with --ddp-overlap)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="p8_64MiB_fp32_ring_ddp_mean")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ddp-buckets", action="store_true",
@@ -160,6 +162,8 @@ def parse_args():
                     help="--ddp-overlap: gradient dtype (bf16: bf16 GEMMs and bf16 bucket all-reduces)")
     ap.add_argument("--comm-priority", action="store_true",
                     help="--ddp-overlap: run the communication stream at the highest priority")
+    ap.add_argument("--no-more-configs", action="store_true",
+                    help="time only the chosen workload (skip the other large configs after it)")
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep (P=8 fp32, 8 B .. 1 GiB per rank) with an alpha-beta fit")
     return ap.parse_args()
@@ -185,8 +189,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, gpu):
+        self.gpu = gpu            # nvidia-smi --id: the GPU's UUID ("GPU-...") or its index
         self.rows = []
         self.proc = None
         self.thread = None
@@ -234,6 +238,118 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(rows),
                 "samples_in_timed_region": len(inside)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    """The device's NVML / nvidia-smi UUID ("GPU-..."), which names the same GPU
+    whatever CUDA_VISIBLE_DEVICES does to the indices; None if unknown."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+class NvmlClocks:
+    """Query-only NVML reads (SM clock, its maximum, the active clock-event
+    reasons) taken by the host while the timed region runs on the GPU: the
+    timed region of a short run is far shorter than nvidia-smi's sampling
+    period.  Changes no setting.  Every method is a no-op if NVML is missing."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str | None, index: int):
+        import ctypes
+
+        self.c = ctypes
+        self.h = None
+        self.samples = []           # (inside the timed region, sm_mhz, reasons bitmask)
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = (L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) if uuid
+                  else L.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)))
+            if rc != 0:
+                return
+            self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                L.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.L, self.h = L, h
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+        except (OSError, AttributeError):
+            self.h = None
+
+    def sample(self, inside: bool):
+        if self.h is None:
+            return
+        c = self.c
+        mhz, bits = c.c_uint(), c.c_ulonglong()
+        if self.L.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) != 0:   # NVML_CLOCK_SM
+            return
+        if self.reasons_fn(self.h, c.byref(bits)) != 0:
+            bits.value = 0
+        self.samples.append((inside, float(mhz.value), int(bits.value)))
+
+    def poll(self, start_ev, end_ev, limit_s: float = 600.0):
+        """Samples until end_ev has completed; a sample counts as inside the
+        timed region when start_ev had completed before it was taken."""
+        t_end = time.time() + limit_s
+        while not end_ev.query() and time.time() < t_end:
+            inside = start_ev.query()
+            self.sample(inside)
+            if self.h is None:
+                time.sleep(0.001)
+
+    def summary(self) -> dict:
+        inside = [x for x in self.samples if x[0]]
+        names = sorted({n for _, _, b in inside for bit, n in self.REASONS.items() if b & bit})
+        return {"samples_in_timed_region": len(inside),
+                "sm_mhz": statistics.median([m for _, m, _ in inside]) if inside else None,
+                "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": names}
+
+
+def merged_clocks(smi: dict, nvml: dict) -> dict:
+    """nvidia-smi's samples around the run and NVML's inside the timed region:
+    the timed region's own figures win where it has any."""
+    out = dict(smi)
+    out["nvidia_smi_samples_in_timed_region"] = smi.get("samples_in_timed_region", 0)
+    if nvml.get("samples_in_timed_region"):
+        out["sm_mhz"] = nvml["sm_mhz"]
+        out["sm_max_mhz"] = nvml["sm_max_mhz"] or smi.get("sm_max_mhz")
+        out["reasons"] = sorted(set(smi.get("reasons", [])) | set(nvml["reasons"]))
+        out["samples_in_timed_region"] = smi.get("samples_in_timed_region", 0) + nvml["samples_in_timed_region"]
+        out["nvml_samples_in_timed_region"] = nvml["samples_in_timed_region"]
+        out["sm_mhz_source"] = "NVML reads while the timed region ran"
+    return out
+
+
+# The timed region starts with a spin kernel queued ahead of the start event:
+# it holds the GPU while the host enqueues the K steps, so the region times the
+# steps themselves -- not the host's issue of the first call (~23 us through
+# ctypes) or the GPU waking from the idle pause before it (a first step of
+# 190-280 us instead of 160 us was measured without it).
+HIDE_CYCLES = 4_000_000   # ~2 ms at 2 GHz
+
+
+def timed_steps(torch, step, steps: int, stream, nvml: "NvmlClocks | None" = None) -> float:
+    """ms for `steps` calls of step(), timed by CUDA events on `stream`."""
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HIDE_CYCLES)
+    torch.cuda.nvtx.range_push("timed")      # lets a profiler select exactly this region
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    if nvml is not None:
+        nvml.poll(ev0, ev1)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1)
 
 
 # ---------------------------------------------------------------- roofline
@@ -492,34 +608,26 @@ def ours_arm(args, w, name):
     def step():
         call(sends, recvs, stream)
 
+    uuid = gpu_uuid(torch, dev)
+    clocks = ClockSampler(uuid or local)
+    clocks.start()
+    nvml = NvmlClocks(uuid, local)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error in warm-up")
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    torch.cuda.nvtx.range_push("timed")      # lets a profiler select exactly this region
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize()
+    ms = timed_steps(torch, step, args.steps, stream, nvml)
     t1 = time.time()
     if dist:
         dist.barrier()
     time.sleep(0.2)
     clocks.stop()
-    ms = ev0.elapsed_time(ev1)
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error in the timed region")
     ms_step = max_over_ranks(ms, dist) / args.steps
@@ -605,13 +713,110 @@ def ours_arm(args, w, name):
                     "path": "pinned host -> device copies, ar_allreduce, device -> pinned host copies "
                             "of all P results; pipelined over 2 buffer sets / 3 streams"},
             "gpu_launches": args.steps,
-            "clocks": clocks.summary(t0, t1),
+            "clocks": merged_clocks(clocks.summary(t0, t1), nvml.summary()),
+            "timing": "CUDA events on the launching stream around the K steps; a ~2 ms spin kernel "
+                      "queued ahead of the start event holds the GPU while the host enqueues them",
         }
-        print(json.dumps(line), flush=True)
     ar.ar_destroy(comm)
+    if line is not None and world == 1 and name == HEADLINE and not args.no_more_configs:
+        del sends, recvs, sets
+        torch.cuda.empty_cache()
+        line["more_configs"] = more_configs(args, dev, stream, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return line
+
+
+# ----------------------------------------------------- the other large configs
+
+MORE_CONFIGS = ("p8_256MiB_bf16_tree", "p72_16MiB_int32_sum_ring", "p72_16MiB_int32_max_tree",
+                "ddp_1p2b_fp32_25MiB_buckets")
+
+
+def more_configs(args, dev, stream, world: int) -> dict:
+    """The other large-message workloads, each timed like the headline (warm-up,
+    a spin ahead of the start event, K steps between CUDA events) in this
+    process after it: 8 x 256 MiB bf16 in the double-binary-tree order, 72
+    ranks x 16 MiB int32 (ring sum, tree max), and the DDP bucket loop (185
+    calls of 25 MiB per step, replayed from one CUDA graph; at most 100 timed
+    steps).  Only after the headline workload at N = 1."""
+    import torch
+
+    import allreduce_reduction_emulated_gb300 as ar
+    import synthetic
+
+    peak, _ = measured_hbm_peak()
+    out = {}
+    for name in MORE_CONFIGS:
+        if name.startswith("ddp_"):
+            P, total, B, sigma, seed = 8, DDP_PARAMS, DDP_BUCKET, 1e-3, 5
+            buckets = [(b, min(B, total - b)) for b in range(0, total, B)]
+            sends = []
+            for r in range(P):
+                flat = torch.empty(total, dtype=torch.float32, device=dev)
+                for start, n in buckets:
+                    flat[start:start + n] = synthetic.values_torch("normal", seed, r, start, n, dev, sigma)
+                sends.append(flat)
+            recvs = [torch.empty_like(x) for x in sends]
+            comm = ar.ar_init(P)
+            views = [([x[a:a + n] for x in sends], [y[a:a + n] for y in recvs], n) for a, n in buckets]
+            side = torch.cuda.Stream()
+
+            def calls(s=None):
+                for sv, rv, n in views:
+                    ar.ar_allreduce(comm, sv, rv, n, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125, s)
+
+            calls(stream)                                   # warm-up outside capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    calls(side)
+            step = g.replay
+            per_rank, esize, launches = total * 4, 4, len(buckets)
+            cfg = {"P": P, "params_per_rank": total, "buckets": len(buckets), "bucket_elems": B,
+                   "dtype": "f32", "op": "sum", "algo": "ring", "scale": 0.125,
+                   "values": f"normal sigma={sigma} seed={seed}",
+                   "launch": f"{len(buckets)} calls per step replayed from one CUDA graph"}
+        else:
+            w = WORKLOADS[name]
+            P, count = w["P"], w["count"]
+            dt = {"f32": ar.AR_FLOAT32, "bf16": ar.AR_BFLOAT16, "i32": ar.AR_INT32}[w["dtype"]]
+            sends = [synthetic.values_torch(w["kind"], w["seed"], r, 0, count, dev, w["sigma"]) for r in range(P)]
+            recvs = [torch.empty_like(x) for x in sends]
+            comm = ar.ar_init(P)
+
+            def step(w=w, sends=sends, recvs=recvs, comm=comm, dt=dt, count=count):
+                ar.ar_allreduce(comm, sends, recvs, count, dt, ar.OPS[w["op"]], ar.ALGOS[w["algo"]],
+                                w["scale"], stream)
+
+            per_rank, esize, launches = count * ESIZE[w["dtype"]], ESIZE[w["dtype"]], 1
+            cfg = {k: w[k] for k in ("P", "dtype", "op", "algo", "scale")}
+            cfg["count_per_rank"] = count
+            cfg["values"] = f"{w['kind']} sigma={w['sigma']} seed={w['seed']}"
+        k = min(args.steps, 100) if name.startswith("ddp_") else args.steps
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        ms = timed_steps(torch, step, k, stream) / k
+        if ar.ar_get_status(comm) != ar.AR_SUCCESS:
+            raise SystemExit(f"device status error in {name}")
+        achieved = 2 * P * per_rank / (ms * 1e-3) / 1e9
+        algbw = job_gbs(per_rank, ms, world)
+        out[name] = {**cfg, "steps": k, "warmup": args.warmup, "ms_per_step": ms,
+                     "algbw": algbw, "busbw": algbw * 2 * (P - 1) / P,
+                     "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                  "frac": achieved / peak, "traffic": profiled_traffic(name)},
+                     "gpu_launches": launches * k}
+        ar.ar_destroy(comm)
+        del sends, recvs, step
+        if name.startswith("ddp_"):
+            del g, views
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ sweep
@@ -756,20 +961,14 @@ def ddp_buckets(args):
         for sv, rv, n in views:
             ar.ar_allreduce(comm, sv, rv, n, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 0.125)
 
-    def timed(fn, k):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record()
-        for _ in range(k):
-            fn()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / k
-
+    uuid = gpu_uuid(torch, dev)
+    clocks = ClockSampler(uuid or 0)
+    clocks.start()
+    nvml = NvmlClocks(uuid, 0)
     for _ in range(args.warmup):
         step()
-    eager_ms = timed(step, args.steps)
+    torch.cuda.synchronize()
+    eager_ms = timed_steps(torch, step, args.steps, stream) / args.steps
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -777,14 +976,11 @@ def ddp_buckets(args):
             step()
     for _ in range(args.warmup):
         g.replay()
-    clocks = ClockSampler(0)
-    clocks.start()
-    time.sleep(0.3)
+    torch.cuda.synchronize()
     t0 = time.time()
-    torch.cuda.nvtx.range_push("timed")
-    graph_ms = timed(g.replay, args.steps)
-    torch.cuda.nvtx.range_pop()
+    graph_ms = timed_steps(torch, g.replay, args.steps, stream, nvml) / args.steps
     t1 = time.time()
+    time.sleep(0.2)
     clocks.stop()
     if ar.ar_get_status(comm) != ar.AR_SUCCESS:
         raise SystemExit("device status error")
@@ -822,7 +1018,7 @@ def ddp_buckets(args):
                          "kind": "oracle",
                          "sample": f"the first {nb_cpu} bucket all-reduces ({done} elements per rank)"},
         "e2e": None, "gpu_launches": len(buckets) * args.steps,
-        "clocks": clocks.summary(t0, t1),
+        "clocks": merged_clocks(clocks.summary(t0, t1), nvml.summary()),
     }
     print(json.dumps(line), flush=True)
 

@@ -136,3 +136,45 @@ def test_sm_time_bound():
     assert bench.sm_time_bound_ms(1.0, 30.0, 8, 152) == 30.0          # never below either side
     assert bench.sm_time_bound_ms(18.4, 11.4, 0, 152) is None          # uncapped: split unknown
     assert bench.sm_time_bound_ms(18.4, 11.4, 152, 152) is None
+
+
+def test_nvml_samples_inside_the_timed_region_win():
+    """Clock samples taken by NVML while the timed region ran replace
+    nvidia-smi's when nvidia-smi had none inside it; reasons are the union."""
+    n = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    n.h, n.max_mhz = None, 2070.0
+    n.samples = [(False, 1500.0, 0x1), (True, 2070.0, 0x0), (True, 2055.0, 0x4), (True, 2070.0, 0x0)]
+    s = n.summary()
+    assert s["samples_in_timed_region"] == 3 and s["sm_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    smi = {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10, "samples_in_timed_region": 0}
+    m = bench.merged_clocks(smi, s)
+    assert m["sm_mhz"] == 2070.0 and m["samples_in_timed_region"] == 3
+    assert m["nvml_samples_in_timed_region"] == 3 and m["reasons"] == ["sw_power_cap"]
+    # no NVML samples: nvidia-smi's figures stand
+    empty = {"samples_in_timed_region": 0, "sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+    assert bench.merged_clocks(smi, empty)["sm_mhz"] == 1980.0
+
+
+def test_nvml_polling_is_a_no_op_without_the_library(monkeypatch):
+    """Without libnvidia-ml the clock reader records nothing and polling ends
+    when the end event completes."""
+    import ctypes
+
+    def missing(name, *a, **k):
+        raise OSError(name)
+
+    monkeypatch.setattr(ctypes, "CDLL", missing)
+    n = bench.NvmlClocks(None, 0)
+    assert n.h is None
+
+    class Ev:
+        def __init__(self, left):
+            self.left = left
+
+        def query(self):
+            self.left -= 1
+            return self.left <= 0
+
+    n.poll(Ev(1), Ev(3))
+    assert n.samples == [] and n.summary()["samples_in_timed_region"] == 0
