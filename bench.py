@@ -334,13 +334,14 @@ def merged_clocks(smi: dict, nvml: dict) -> dict:
 HIDE_CYCLES = 4_000_000   # ~2 ms at 2 GHz
 
 
-def timed_steps(torch, step, steps: int, stream, nvml: "NvmlClocks | None" = None) -> float:
+def timed_steps(torch, step, steps: int, stream, nvml: "NvmlClocks | None" = None,
+                range_name: str = "timed") -> float:
     """ms for `steps` calls of step(), timed by CUDA events on `stream`."""
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         torch.cuda._sleep(HIDE_CYCLES)
-    torch.cuda.nvtx.range_push("timed")      # lets a profiler select exactly this region
+    torch.cuda.nvtx.range_push(range_name)   # lets a profiler select exactly this region
     ev0.record(stream)
     for _ in range(steps):
         step()
@@ -800,7 +801,7 @@ def more_configs(args, dev, stream, world: int) -> dict:
         for _ in range(args.warmup):
             step()
         torch.cuda.synchronize()
-        ms = timed_steps(torch, step, k, stream) / k
+        ms = timed_steps(torch, step, k, stream, range_name=f"more_configs {name}") / k
         if ar.ar_get_status(comm) != ar.AR_SUCCESS:
             raise SystemExit(f"device status error in {name}")
         achieved = 2 * P * per_rank / (ms * 1e-3) / 1e9
@@ -881,7 +882,7 @@ def sweep(args):
                 # host's issue time is not inside the events; "us_with_issue":
                 # the events bracket the host's issue of the call as well
                 times, issued = [], []
-                for _ in range(50):
+                for _ in range(100):
                     for hide, out in ((True, times), (False, issued)):
                         flush.zero_()
                         a = torch.cuda.Event(enable_timing=True)
@@ -894,6 +895,7 @@ def sweep(args):
                         torch.cuda.synchronize()
                         out.append(a.elapsed_time(b))
                 t = statistics.median(times) * 1e-3
+                t_mean = statistics.fmean(times) * 1e-3
                 t_issue = statistics.median(issued) * 1e-3
             else:
                 iters = max(5, min(200, int(2e9 / (2 * P * nbytes))))
@@ -905,11 +907,13 @@ def sweep(args):
                 b.record(stream)
                 torch.cuda.synchronize()
                 t = a.elapsed_time(b) * 1e-3 / iters
+                t_mean = t
             if ar.ar_get_status(comm) != ar.AR_SUCCESS:
                 raise SystemExit("device status error in the sweep")
             rows.append({"bytes_per_rank": nbytes, "algo": names[algo],
                          "resolved": names[ar.ar_select_algo(comm, count, ar.AR_FLOAT32, algo)],
-                         "us": t * 1e6, "us_with_issue": None if t_issue is None else t_issue * 1e6,
+                         "us": t * 1e6, "us_mean": t_mean * 1e6,
+                         "us_with_issue": None if t_issue is None else t_issue * 1e6,
                          "algbw": nbytes / t / 1e9,
                          "busbw": nbytes / t / 1e9 * 2 * (P - 1) / P,
                          "hbm_gbs": 2 * P * nbytes / t / 1e9, "l2_flushed": small})
@@ -917,8 +921,10 @@ def sweep(args):
     table = ar.ar_tune(comm)
     ar.ar_destroy(comm)
     fits = {}
+    # fitted on the per-point means: the event timer steps by about 2 us, so
+    # single calls (and their medians) are quantized, their means are not
     for name in ("ring", "tree", "ll", "ll128", "auto"):
-        pts = [(r["bytes_per_rank"], r["us"] * 1e-6) for r in rows if r["algo"] == name]
+        pts = [(r["bytes_per_rank"], r["us_mean"] * 1e-6) for r in rows if r["algo"] == name]
         if len(pts) >= 2:
             alpha, beta = fit_alpha_beta(pts)
             fits[name] = {"alpha_us": alpha * 1e6, "inv_beta_gbs": (1 / beta / 1e9) if beta > 0 else None,

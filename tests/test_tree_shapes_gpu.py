@@ -60,7 +60,8 @@ def test_tree_and_ring_orders_for_many_ranks(P, dev):
 @pytest.mark.parametrize("P", [17, 129, 256])
 def test_ll_protocols_at_many_ranks(P, dev):
     """LL and LL128 with up to AR_MAX_RANKS ranks (the widest parameter block;
-    every rank's block group resident at once), against the oracle's ring."""
+    LL stages several words per thread above 8 ranks, LL128 keeps every
+    rank's block group resident at once), against the oracle's ring."""
     rng = np.random.default_rng(700 + P)
     comm = ar.ar_init(P)
     try:
