@@ -31,6 +31,8 @@ AR_ALGO_AUTO, AR_ALGO_RING, AR_ALGO_TREE, AR_ALGO_LL, AR_ALGO_HIER, AR_ALGO_LL12
 (AR_OPT_LL_MAX_BYTES, AR_OPT_LL_SPIN_LIMIT, AR_OPT_DEBUG, AR_OPT_LL_SKIP_PRODUCER, AR_OPT_HIER_GROUP,
  AR_OPT_MAX_BLOCKS, AR_OPT_LL128_MAX_BYTES, AR_OPT_AUTO_TUNED) = range(8)
 AR_OPT_LL_EPOCH = 8
+AR_OPT_CAPPED_KERNEL = 9
+AR_CAPPED_WIDE, AR_CAPPED_TMA = 0, 1
 AR_TUNE_BUCKETS = 22
 AR_MAX_RANKS = 256
 AR_NOALLOC_MAX_RANKS, AR_NOALLOC_MAX_BYTES = 8, 65536

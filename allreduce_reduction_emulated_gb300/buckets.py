@@ -17,7 +17,8 @@ from __future__ import annotations
 
 import torch
 
-from . import AR_ALGO_RING, AR_OPT_MAX_BLOCKS, AR_SUM, ar_allreduce, ar_set_option, dtype_of
+from . import (AR_ALGO_RING, AR_CAPPED_TMA, AR_OPT_CAPPED_KERNEL, AR_OPT_MAX_BLOCKS, AR_SUM, ar_allreduce,
+               ar_set_option, dtype_of)
 
 # Share of the SMs that max_blocks="auto" gives the all-reduces.  Measured on
 # GB300 (152 SMs) with the bucket all-reduces of a 1.2B-parameter backward
@@ -45,12 +46,17 @@ class BucketReducer:
     out       optional P result tensors (default: reduce in place)
     max_blocks    if given, AR_OPT_MAX_BLOCKS is set to it on the communicator
                   before each bucket's all-reduce: the all-reduces then run on a
-                  few SMs (the TMA pipeline) beside the backward pass; "auto"
-                  takes AUTO_SM_FRACTION of the gradients' GPU's SMs
+                  few SMs beside the backward pass; "auto" takes
+                  AUTO_SM_FRACTION of the gradients' GPU's SMs
+    capped_kernel AR_OPT_CAPPED_KERNEL set with max_blocks (default: the TMA
+                  pipeline -- beside the gradient GEMMs it gave 25.1 ms per step
+                  on 48 SMs against 27.7 ms for the wide load/store kernel,
+                  which is the faster of the two when nothing else runs)
     """
 
     def __init__(self, comm: int, grads, bucket: int, scale: float = 1.0, algo: int = AR_ALGO_RING,
-                 out=None, stream: torch.cuda.Stream | None = None, max_blocks: int | str | None = None):
+                 out=None, stream: torch.cuda.Stream | None = None, max_blocks: int | str | None = None,
+                 capped_kernel: int = AR_CAPPED_TMA):
         self.comm = comm
         self.grads = list(grads)
         self.out = list(out) if out is not None else self.grads
@@ -67,6 +73,7 @@ class BucketReducer:
         elif max_blocks is not None and not isinstance(max_blocks, int):
             raise ValueError(f"max_blocks must be an int, 'auto' or None, not {max_blocks!r}")
         self.max_blocks = max_blocks
+        self.capped_kernel = capped_kernel
 
     def reset(self):
         self.next_bucket = 0
@@ -84,6 +91,7 @@ class BucketReducer:
                 self.stream.wait_event(event)
             if self.max_blocks is not None:
                 ar_set_option(self.comm, AR_OPT_MAX_BLOCKS, self.max_blocks)
+                ar_set_option(self.comm, AR_OPT_CAPPED_KERNEL, self.capped_kernel)
             ar_allreduce(self.comm, [g[s:e] for g in self.grads], [o[s:e] for o in self.out], e - s,
                          self.dtype, AR_SUM, self.algo, self.scale, self.stream)
             self.next_bucket += 1

@@ -44,6 +44,10 @@ struct ar_comm {
   int tuned_valid = 0;
   int auto_tuned = 0;
   int max_blocks = 0;            // AR_OPT_MAX_BLOCKS (0 = no cap)
+  // AR_OPT_CAPPED_KERNEL: kernel for P <= 8 ring / tree all-reduces and
+  // reduce-scatters capped below the SM count (0 = the wide load/store shape,
+  // 1 = the TMA pipeline; initial value from AR_CAPPED_KERNEL=wide|tma)
+  int capped_tma = 0;
 };
 
 namespace {
@@ -287,6 +291,10 @@ ar_status_t ar_init(int nranks, ar_comm_t* out) {
   long long spin = env_ll("AR_LL_SPIN_LIMIT", (long long)kDefaultSpinLimit);
   c->spin_limit = (uint32_t)std::min<long long>(std::max<long long>(spin, 1), 0xffffffffll);
   c->debug = (int)env_ll("AR_DEBUG", 0);
+  {
+    const char* k = std::getenv("AR_CAPPED_KERNEL");
+    c->capped_tma = (k && std::strcmp(k, "tma") == 0) ? 1 : 0;
+  }
 
   c->stage_stride = (c->ll_capacity_bytes + 3) / 4 + 4;
   const size_t stage_bytes = (size_t)nranks * c->stage_stride * sizeof(unsigned long long);
@@ -375,6 +383,10 @@ ar_status_t ar_set_option(ar_comm_t c, ar_option_t option, long long value) {
       if (value < 0 || value > 0x7fffffffll) return AR_ERR_INVALID_ARG;
       c->max_blocks = (int)value;
       return AR_SUCCESS;
+    case AR_OPT_CAPPED_KERNEL:
+      if (value != AR_CAPPED_WIDE && value != AR_CAPPED_TMA) return AR_ERR_INVALID_ARG;
+      c->capped_tma = value == AR_CAPPED_TMA;
+      return AR_SUCCESS;
     case AR_OPT_HIER_GROUP:
       if (value < 1 || value > c->P || c->P % value != 0) return AR_ERR_INVALID_ARG;
       c->hier_group = (int)value;
@@ -460,10 +472,15 @@ ar_status_t ar_allreduce(ar_comm_t c, const void* const* sendbufs, void* const* 
     e = ar::launch_ll128(call, &info);
   } else if (chosen == AR_ALGO_HIER) {
     e = ar::launch_generic(call, &info);
+  } else if (P <= ar::kMaxStaticRanks && c->max_blocks > 0 && c->max_blocks < c->sms && !c->capped_tma) {
+    // capped to fewer SMs than the GPU has: 1024-thread blocks, one per SM,
+    // keep twice the bytes in flight per SM of the 256-thread shape
+    e = dtype == AR_FLOAT32    ? ar::launch_wide_f32(call, &info)
+        : dtype == AR_BFLOAT16 ? ar::launch_wide_bf16(call, &info)
+                               : ar::launch_wide_i32(call, &info);
   } else if (P <= ar::kMaxStaticRanks && c->max_blocks > 0 && c->max_blocks < c->sms &&
              count * esize / ar::kTmaTileBytes >= (size_t)c->max_blocks) {
-    // capped to fewer SMs than the GPU has, with at least a tile per block:
-    // the TMA pipeline keeps far more bytes in flight per SM
+    // (AR_CAPPED_KERNEL=tma) capped, with at least a tile per block: the TMA pipeline
     e = dtype == AR_FLOAT32    ? ar::launch_tma_f32(call, &info)
         : dtype == AR_BFLOAT16 ? ar::launch_tma_bf16(call, &info)
                                : ar::launch_tma_i32(call, &info);
@@ -511,9 +528,14 @@ ar_status_t ar_reduce_scatter(ar_comm_t c, const void* const* sendbufs, void* co
   cudaError_t e;
   if (!vec) {
     e = ar::launch_reduce_scatter_elem(call, &info);
+  } else if (c->P <= ar::kMaxStaticRanks && c->max_blocks > 0 && c->max_blocks < c->sms && !c->capped_tma) {
+    // capped to fewer SMs than the GPU has: the wide shape, shard-owner stores
+    e = dtype == AR_FLOAT32    ? ar::launch_wide_f32(call, &info)
+        : dtype == AR_BFLOAT16 ? ar::launch_wide_bf16(call, &info)
+                               : ar::launch_wide_i32(call, &info);
   } else if (c->P <= ar::kMaxStaticRanks && c->max_blocks > 0 && c->max_blocks < c->sms &&
              call.count * ar::elem_bytes(dtype) / ar::kTmaTileBytes >= (size_t)c->max_blocks) {
-    // capped to fewer SMs than the GPU has: the TMA pipeline, shard-owner stores
+    // (AR_CAPPED_KERNEL=tma) the TMA pipeline, shard-owner stores
     e = dtype == AR_FLOAT32    ? ar::launch_tma_f32(call, &info)
         : dtype == AR_BFLOAT16 ? ar::launch_tma_bf16(call, &info)
                                : ar::launch_tma_i32(call, &info);

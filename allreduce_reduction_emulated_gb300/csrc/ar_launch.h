@@ -59,6 +59,11 @@ inline size_t elem_bytes(int dtype) { return dtype == 1 ? 2 : 4; }
 cudaError_t launch_static_f32(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_bf16(const Call& c, LaunchInfo* info);
 cudaError_t launch_static_i32(const Call& c, LaunchInfo* info);
+// the same kernels in their wide shape (1024 threads per block, at most
+// c.max_blocks blocks and one per SM, grid-stride): for calls that share the GPU
+cudaError_t launch_wide_f32(const Call& c, LaunchInfo* info);
+cudaError_t launch_wide_bf16(const Call& c, LaunchInfo* info);
+cudaError_t launch_wide_i32(const Call& c, LaunchInfo* info);
 // the same all-reduce (P <= kMaxStaticRanks, ring or tree; or the ring
 // reduce-scatter when c.shard != 0) as a TMA bulk-copy pipeline, one block per
 // SM on c.max_blocks SMs: for calls that share the GPU

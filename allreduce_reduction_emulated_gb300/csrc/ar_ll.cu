@@ -33,7 +33,8 @@ namespace ar {
 
 namespace {
 
-constexpr int kLLThreads = 256;
+constexpr int kLLThreads = 256;   // threads that stage and receive words
+constexpr int kLLBlock = kLLThreads + 32;  // + one warp that counts the block into the epoch
 constexpr int kLLBatch = 8;       // staged words polled together (loads in flight)
 constexpr int kLLMinSlice = 32;   // words per block when P >= 8 (one staged word per thread)
 
@@ -154,7 +155,8 @@ __device__ __forceinline__ void ll_reduce_slice(const LLParams<MAXP>& p, uint64_
 }
 
 template <int MAXP, int DT, int OP>
-__global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_constant__ LLParams<MAXP> p) {
+__global__ void __launch_bounds__(kLLBlock) ll_allreduce_kernel(const __grid_constant__ LLParams<MAXP> p) {
+  const bool worker = threadIdx.x < kLLThreads;
   const uint64_t base = (uint64_t)blockIdx.x * (uint64_t)p.slice_words;
   const uint64_t left = p.nwords - base;
   const uint32_t nb = left < (uint64_t)p.slice_words ? (uint32_t)left : (uint32_t)p.slice_words;
@@ -162,15 +164,18 @@ __global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_c
   // staged word i is rank i / nb's word base + i % nb (consecutive threads read
   // consecutive words of one rank); the first is loaded while thread 0 reads
   // the epoch
-  const bool first = !p.skip_produce && threadIdx.x < nstage;
+  const bool first = !p.skip_produce && worker && threadIdx.x < nstage;
   const uint32_t r0 = first ? threadIdx.x / nb : 0u;
   const uint64_t w0 = base + (threadIdx.x - r0 * nb);
   const uint32_t v0 = first ? load_payload(p.send[r0], w0, p.nbytes) : 0u;
   const uint32_t epoch = ll_epoch_begin(p.epoch_state);
   const unsigned long long tag = (unsigned long long)epoch << 32;
 
+  // the extra warp counts the block in at once (ll_epoch_arrive: any time after
+  // ll_epoch_begin), so its fence and atomic overlap the staging and polling
+  if (threadIdx.x == kLLThreads) ll_epoch_arrive(p.epoch_state, epoch);
   // produce: stage the P ranks' payload words of this slice with this call's flag
-  if (!p.skip_produce) {
+  if (!p.skip_produce && worker) {
     if (first) st_relaxed_u64(p.staging + (uint64_t)r0 * p.stride + w0, tag | v0);
     // more than 8 ranks: further words, their loads issued four at a time
     for (uint32_t i0 = threadIdx.x + kLLThreads; i0 < nstage; i0 += 4 * kLLThreads) {
@@ -193,10 +198,7 @@ __global__ void __launch_bounds__(kLLThreads) ll_allreduce_kernel(const __grid_c
       }
     }
   }
-  // counted in by the block's last thread, which receives no word when the
-  // slice is shorter than the block
-  if (threadIdx.x == kLLThreads - 1) ll_epoch_arrive(p.epoch_state, epoch);
-  ll_reduce_slice<MAXP, DT, OP>(p, base, nb, epoch);
+  if (worker) ll_reduce_slice<MAXP, DT, OP>(p, base, nb, epoch);
   ll_epoch_end(p.epoch_state, epoch, p.staging, p.stage_words);
 }
 
@@ -227,11 +229,11 @@ cudaError_t launch_ll_one(const Call& c, LaunchInfo* info) {
   p.slice_words = slice;
   const uint64_t grid = (p.nwords + (uint64_t)slice - 1) / (uint64_t)slice;
   if (grid == 0 || grid > 0x7fffffffull) return cudaErrorInvalidValue;
-  kernel<<<(unsigned)grid, kLLThreads, 0, c.stream>>>(p);
+  kernel<<<(unsigned)grid, kLLBlock, 0, c.stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   info->kernel = "ll";
   info->grid = (int)grid;
-  info->block = kLLThreads;
+  info->block = kLLBlock;
   info->smem = 0;
   return e;
 }

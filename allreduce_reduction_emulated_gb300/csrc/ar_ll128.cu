@@ -8,9 +8,13 @@
 // memory model, so the line is published explicitly: the lanes of a warp
 // write the payload words, fence, synchronise, and one lane stores the flag
 // word with release semantics; a reader acquires the flag and only then reads
-// the payload.  Emulated like LL inside one cooperative kernel: block group g
-// stages rank g's lines, then reduces ring chunk g in ring order (so LL128 ==
-// RING bit for bit) and writes the result into every rank's receive buffer.
+// the payload.  Emulated like LL, one block per slice of the message: block b
+// owns lines [b * S, (b + 1) * S) of every rank (S = the slice, 4 lines for 8
+// ranks); its warps play the P ranks and stage those lines, then its threads
+// receive the slice's payload words -- each acquires the flag of its word's
+// line in every rank's slot, reads the word and folds the P values in ring
+// order (so LL128 == RING bit for bit) -- and write the result into every
+// rank's receive buffer.  No block waits for another block.
 // The epoch is kept on the device as for LL, so calls can be captured in a
 // CUDA graph.  Every flag wait is bounded; on its limit a thread records
 // AR_ERR_TIMEOUT and stops reducing.
@@ -23,10 +27,13 @@ namespace ar {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;      // threads that stage and receive lines
+constexpr int kBlock = kThreads + 32;  // + one warp that counts the block into the epoch
 constexpr int kLineWords = 16;     // 8-byte words per 128-byte line
 constexpr int kPayloadWords = 15;  // the 16th word is the flag
 constexpr int kBatch = 8;          // ranks polled together
+constexpr int kWarpLines = 4;      // lines a warp stages at once (8 lanes per line)
+constexpr int kRoundLines = kThreads / 32 * kWarpLines;  // lines a block stages at once
 
 template <int MAXP>
 struct LL128Params {
@@ -43,7 +50,7 @@ struct LL128Params {
   uint64_t stage_words;  // whole staging area (P slots), cleared on epoch wrap
   uint32_t spin_limit;
   int P;
-  int bpr;
+  int slice_lines;       // lines of every rank per block
   int skip_produce;
   int do_scale;
   float scale;
@@ -122,19 +129,19 @@ __device__ __forceinline__ unsigned long long narrow8(Word8<DT> a, float scale, 
   }
 }
 
-// Reduces ring chunk g, one 8-byte payload word per thread per step, and
-// writes it to every rank; returns early (status AR_ERR_TIMEOUT) if a flag
-// wait runs out.
+// Receives the payload words of lines [l0, l0 + nl) of every rank, one word
+// per thread per step: acquires the flag of the word's line in each rank's
+// slot, reads the word, folds in ring order and writes the result to every
+// rank; returns early (status AR_ERR_TIMEOUT) if a flag wait runs out.
 template <int MAXP, int DT, int OP>
-__device__ __forceinline__ void ll128_reduce_chunk(const LL128Params<MAXP>& p, int g,
+__device__ __forceinline__ void ll128_reduce_slice(const LL128Params<MAXP>& p, uint64_t l0, uint32_t nl,
                                                    unsigned long long flag) {
   const int P = p.P;
-  const uint64_t lt = (uint64_t)(blockIdx.x % p.bpr) * kThreads + threadIdx.x;
-  const uint64_t nt = (uint64_t)p.bpr * kThreads;
-  const uint64_t w0 = (uint64_t)g * p.chunk_words;
-  uint64_t w1 = w0 + p.chunk_words;
-  if (w1 > p.nwords) w1 = p.nwords;
-  for (uint64_t w = w0 + lt; w < w1; w += nt) {
+  const uint64_t wa = l0 * kPayloadWords;
+  uint64_t wb = wa + (uint64_t)nl * kPayloadWords;
+  if (wb > p.nwords) wb = p.nwords;
+  for (uint64_t w = wa + threadIdx.x; w < wb; w += kThreads) {
+    const int g = (int)(w / p.chunk_words);  // ring chunk: folded from rank g
     const uint64_t line = w / kPayloadWords;
     const uint64_t off = line * kLineWords + (w - line * kPayloadWords);
     Word8<DT> acc;
@@ -175,39 +182,57 @@ __device__ __forceinline__ void ll128_reduce_chunk(const LL128Params<MAXP>& p, i
 }
 
 template <int MAXP, int DT, int OP>
-__global__ void __launch_bounds__(kThreads) ll128_allreduce_kernel(const __grid_constant__ LL128Params<MAXP> p) {
-  const int g = blockIdx.x / p.bpr;
+__global__ void __launch_bounds__(kBlock) ll128_allreduce_kernel(const __grid_constant__ LL128Params<MAXP> p) {
+  const bool worker = threadIdx.x < kThreads;
   const int lane = threadIdx.x & 31;
+  const int part = lane & 7;  // 16-byte part of a line
+  const uint64_t l0 = (uint64_t)blockIdx.x * (uint64_t)p.slice_lines;
+  const uint64_t left = p.nlines - l0;
+  const uint32_t nl = left < (uint64_t)p.slice_lines ? (uint32_t)left : (uint32_t)p.slice_lines;
+  const uint32_t nstage = (uint32_t)p.P * nl;  // lines this block stages: P ranks x nl
+  // block line i is rank i / nl's line l0 + i % nl; a warp stages 4 lines at a
+  // time, 8 lanes (16 bytes each) per line.  The first round's payload words
+  // are loaded while thread 0 reads the epoch.
+  const uint32_t i0 = (threadIdx.x >> 5) * kWarpLines + (uint32_t)(lane >> 3);
+  unsigned long long a = 0, b = 0;
+  const bool live0 = !p.skip_produce && worker && i0 < nstage;
+  if (live0) {
+    const uint32_t r = i0 / nl;
+    const uint64_t w = (l0 + (i0 - r * nl)) * kPayloadWords + 2 * part;
+    a = w < p.nwords ? load_word8(p.send[r], w, p.nbytes) : 0ull;
+    b = part < 7 && w + 1 < p.nwords ? load_word8(p.send[r], w + 1, p.nbytes) : 0ull;
+  }
   const uint32_t epoch = ll_epoch_begin(p.epoch_state);
   const unsigned long long flag = (unsigned long long)epoch;
 
-  // produce: a warp writes 4 lines at a time, 8 lanes per line (16 bytes
-  // each); lane 7 of each line then publishes the line with its flag word
-  if (!p.skip_produce) {
-    unsigned long long* slot = p.staging + (uint64_t)g * p.stride;
-    const uint64_t warps = (uint64_t)p.bpr * (kThreads / 32);
-    const uint64_t warp = (uint64_t)(blockIdx.x % p.bpr) * (kThreads / 32) + threadIdx.x / 32;
-    const int part = lane & 7;  // 16-byte part of the line
-    for (uint64_t base = warp * 4; base < p.nlines; base += warps * 4) {
-      const uint64_t line = base + (uint64_t)(lane >> 3);
-      const bool live = line < p.nlines;
-      const uint64_t w0 = line * kPayloadWords + 2 * part;  // payload words of this part
+  // the extra warp counts the block in at once (ll_epoch_arrive: any time after
+  // ll_epoch_begin), so its fence and atomic overlap the staging and polling
+  if (threadIdx.x == kThreads) ll_epoch_arrive(p.epoch_state, epoch);
+  // produce: each line's payload words, then (after a fence and the warp
+  // barrier) its flag word stored with release by the line's lane 7 -- a
+  // reader that acquires the flag sees the whole line
+  if (!p.skip_produce && worker) {
+    for (uint32_t i = i0; i - (uint32_t)(lane >> 3) < nstage; i += kRoundLines) {
+      const bool live = i < nstage;
+      const uint32_t r = live ? i / nl : 0u;
+      const uint64_t line = l0 + (i - r * nl);
+      unsigned long long* slot = p.staging + (uint64_t)r * p.stride + line * kLineWords;
       if (live) {
-        slot[line * kLineWords + 2 * part] = w0 < p.nwords ? load_word8(p.send[g], w0, p.nbytes) : 0ull;
-        if (part < 7)
-          slot[line * kLineWords + 2 * part + 1] =
-              w0 + 1 < p.nwords ? load_word8(p.send[g], w0 + 1, p.nbytes) : 0ull;
+        if (i != i0) {
+          const uint64_t w = line * kPayloadWords + 2 * part;
+          a = w < p.nwords ? load_word8(p.send[r], w, p.nbytes) : 0ull;
+          b = part < 7 && w + 1 < p.nwords ? load_word8(p.send[r], w + 1, p.nbytes) : 0ull;
+        }
+        slot[2 * part] = a;
+        if (part < 7) slot[2 * part + 1] = b;
       }
       __threadfence();  // each lane's payload words before the warp barrier ...
       __syncwarp();
-      // ... and the flag after it, with release: a reader that acquires the
-      // flag sees the whole line
-      if (live && part == 7) st_release_u64(slot + line * kLineWords + kPayloadWords, flag);
+      if (live && part == 7) st_release_u64(slot + kPayloadWords, flag);  // ... and the flag after it
     }
   }
 
-  if (threadIdx.x == kThreads - 1) ll_epoch_arrive(p.epoch_state, epoch);
-  ll128_reduce_chunk<MAXP, DT, OP>(p, g, flag);
+  if (worker) ll128_reduce_slice<MAXP, DT, OP>(p, l0, nl, flag);
   ll_epoch_end(p.epoch_state, epoch, p.staging, p.stage_words);
 }
 
@@ -234,25 +259,17 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   p.scale = c.scale;
   if (p.nlines * kLineWords > p.stride) return cudaErrorInvalidValue;
-  static const int blocks_per_sm = [&] {
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess) b = 0;
-    return b;
-  }();
-  const int resident = blocks_per_sm * c.sms;
-  if (c.P > resident) return cudaErrorCooperativeLaunchTooLarge;
-  uint64_t bpr = (p.nlines * 8 + kThreads - 1) / kThreads;  // 8 lanes per line when producing
-  const uint64_t bpr_cap = (uint64_t)(resident / c.P);
-  if (bpr > bpr_cap) bpr = bpr_cap;
-  if (bpr < 1) bpr = 1;
-  p.bpr = (int)bpr;
-  const int grid = c.P * p.bpr;
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchCooperativeKernel((const void*)kernel, dim3(grid), dim3(kThreads), args, 0,
-                                              c.stream);
+  // the 8 warps stage 32 lines at once: 4 lines of each of 8 ranks, more for fewer ranks
+  int slice = kRoundLines / (c.P < 1 ? 1 : c.P);
+  if (slice < kWarpLines) slice = kWarpLines;
+  p.slice_lines = slice;
+  const uint64_t grid = (p.nlines + (uint64_t)slice - 1) / (uint64_t)slice;
+  if (grid == 0 || grid > 0x7fffffffull) return cudaErrorInvalidValue;
+  kernel<<<(unsigned)grid, kBlock, 0, c.stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
   info->kernel = "ll128";
-  info->grid = grid;
-  info->block = kThreads;
+  info->grid = (int)grid;
+  info->block = kBlock;
   info->smem = 0;
   return e;
 }

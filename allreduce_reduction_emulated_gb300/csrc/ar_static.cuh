@@ -94,20 +94,28 @@ __device__ __forceinline__ Acc<DT> reduce_vec(const uint4 (&r)[NP], uint64_t v, 
   }
 }
 
+// The wide shape for calls capped to a few SMs (AR_OPT_MAX_BLOCKS): blocks of
+// 1024 threads, one vector per rank per thread in flight, one block per SM and
+// a grid-stride loop.  A 256-thread block keeps 256 * 2 * NP vectors in
+// flight and moves about 45 GB/s per SM; 1024 threads keep twice that and
+// measured ~100 GB/s per SM for the 8-rank reduce-scatter on 64 SMs.
+constexpr int kWideThreads = 1024;
+constexpr int kWideUnroll = 1;
+
 // SCATTER (ring only): recv[c] is shard c's owner buffer, written at the
 // shard-relative position; there is no partial trailing vector.
-template <int NP, int DT, int OP, int ALGO, bool SCATTER = false>
-__global__ void __launch_bounds__(kStaticThreads)
+template <int NP, int DT, int OP, int ALGO, bool SCATTER = false, int THREADS = kStaticThreads,
+          int U = kStaticUnroll>
+__global__ void __launch_bounds__(THREADS)
     static_allreduce_kernel(const __grid_constant__ StaticParams<NP> p) {
-  constexpr int U = kStaticUnroll;
   const uint64_t n = p.nfull;
-  const uint64_t step = (uint64_t)gridDim.x * (kStaticThreads * U);
-  for (uint64_t base = (uint64_t)blockIdx.x * (kStaticThreads * U) + threadIdx.x; base < n;
+  const uint64_t step = (uint64_t)gridDim.x * (THREADS * U);
+  for (uint64_t base = (uint64_t)blockIdx.x * (THREADS * U) + threadIdx.x; base < n;
        base += step) {
     uint4 r[U][NP];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint64_t v = base + (uint64_t)u * kStaticThreads;
+      const uint64_t v = base + (uint64_t)u * THREADS;
       if (v < n) {
 #pragma unroll
         for (int k = 0; k < NP; ++k) r[u][k] = ld_stream(p.send[k] + v);
@@ -115,7 +123,7 @@ __global__ void __launch_bounds__(kStaticThreads)
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint64_t v = base + (uint64_t)u * kStaticThreads;
+      const uint64_t v = base + (uint64_t)u * THREADS;
       if (v < n) {
         if constexpr (SCATTER) {
           const int c = chunk_of(v, p.split);
@@ -141,10 +149,12 @@ __global__ void __launch_bounds__(kStaticThreads)
   }
 }
 
-template <int DT, int NP, int OP, int ALGO, bool SCATTER = false>
+// WIDE: the 1024-thread shape, grid capped at c.max_blocks and the SM count.
+template <int DT, int NP, int OP, int ALGO, bool SCATTER = false, bool WIDE = false>
 cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
-  constexpr int U = kStaticUnroll;
-  auto kernel = static_allreduce_kernel<NP, DT, OP, ALGO, SCATTER>;
+  constexpr int U = WIDE ? kWideUnroll : kStaticUnroll;
+  constexpr int kThreads = WIDE ? kWideThreads : kStaticThreads;
+  auto kernel = static_allreduce_kernel<NP, DT, OP, ALGO, SCATTER, kThreads, U>;
   StaticParams<NP> p;
   for (int k = 0; k < NP; ++k) {
     p.send[k] = static_cast<const uint4*>(c.send[k]);
@@ -163,55 +173,56 @@ cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   static const int blocks_per_sm = [&] {
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kStaticThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess)
       b = 1;
     return b > 0 ? b : 1;
   }();
-  const uint64_t need = (p.nfull + kStaticThreads * U - 1) / (kStaticThreads * U);
-  uint64_t cap = kStaticPersistent ? (uint64_t)c.sms * (uint64_t)blocks_per_sm : 0x7fffffffull;
+  const uint64_t need = (p.nfull + kThreads * U - 1) / (kThreads * U);
+  uint64_t cap = kStaticPersistent || WIDE ? (uint64_t)c.sms * (uint64_t)blocks_per_sm : 0x7fffffffull;
   if (c.max_blocks > 0 && (uint64_t)c.max_blocks < cap) cap = (uint64_t)c.max_blocks;
   const int grid = (int)(need < 1 ? 1 : (need < cap ? need : cap));
-  kernel<<<grid, kStaticThreads, 0, c.stream>>>(p);
-  info->kernel = SCATTER ? "static_reduce_scatter" : ALGO == kRing ? "static_ring" : "static_tree";
+  kernel<<<grid, kThreads, 0, c.stream>>>(p);
+  info->kernel = WIDE ? (SCATTER ? "wide_reduce_scatter" : ALGO == kRing ? "wide_ring" : "wide_tree")
+                      : (SCATTER ? "static_reduce_scatter" : ALGO == kRing ? "static_ring" : "static_tree");
   info->grid = grid;
-  info->block = kStaticThreads;
+  info->block = kThreads;
   info->smem = 0;
   return cudaGetLastError();
 }
 
-template <int DT, int NP>
+template <int DT, int NP, bool WIDE>
 cudaError_t launch_static_np(const Call& c, LaunchInfo* info) {
   if (c.shard != 0) {  // reduce-scatter
     switch (c.op) {
-      case kSum: return launch_static_one<DT, NP, kSum, kRing, true>(c, info);
-      case kMin: return launch_static_one<DT, NP, kMin, kRing, true>(c, info);
-      case kMax: return launch_static_one<DT, NP, kMax, kRing, true>(c, info);
+      case kSum: return launch_static_one<DT, NP, kSum, kRing, true, WIDE>(c, info);
+      case kMin: return launch_static_one<DT, NP, kMin, kRing, true, WIDE>(c, info);
+      case kMax: return launch_static_one<DT, NP, kMax, kRing, true, WIDE>(c, info);
       default: return cudaErrorInvalidValue;
     }
   }
   const int key = c.op * 4 + c.algo;
   switch (key) {
-    case kSum * 4 + kRing: return launch_static_one<DT, NP, kSum, kRing>(c, info);
-    case kSum * 4 + kTree: return launch_static_one<DT, NP, kSum, kTree>(c, info);
-    case kMin * 4 + kRing: return launch_static_one<DT, NP, kMin, kRing>(c, info);
-    case kMin * 4 + kTree: return launch_static_one<DT, NP, kMin, kTree>(c, info);
-    case kMax * 4 + kRing: return launch_static_one<DT, NP, kMax, kRing>(c, info);
-    case kMax * 4 + kTree: return launch_static_one<DT, NP, kMax, kTree>(c, info);
+    case kSum * 4 + kRing: return launch_static_one<DT, NP, kSum, kRing, false, WIDE>(c, info);
+    case kSum * 4 + kTree: return launch_static_one<DT, NP, kSum, kTree, false, WIDE>(c, info);
+    case kMin * 4 + kRing: return launch_static_one<DT, NP, kMin, kRing, false, WIDE>(c, info);
+    case kMin * 4 + kTree: return launch_static_one<DT, NP, kMin, kTree, false, WIDE>(c, info);
+    case kMax * 4 + kRing: return launch_static_one<DT, NP, kMax, kRing, false, WIDE>(c, info);
+    case kMax * 4 + kTree: return launch_static_one<DT, NP, kMax, kTree, false, WIDE>(c, info);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int DT>
+template <int DT, bool WIDE = false>
 cudaError_t launch_static_dt(const Call& c, LaunchInfo* info) {
   switch (c.P) {
-    case 1: return launch_static_np<DT, 1>(c, info);
-    case 2: return launch_static_np<DT, 2>(c, info);
-    case 3: return launch_static_np<DT, 3>(c, info);
-    case 4: return launch_static_np<DT, 4>(c, info);
-    case 5: return launch_static_np<DT, 5>(c, info);
-    case 6: return launch_static_np<DT, 6>(c, info);
-    case 7: return launch_static_np<DT, 7>(c, info);
-    case 8: return launch_static_np<DT, 8>(c, info);
+    case 1: return launch_static_np<DT, 1, WIDE>(c, info);
+    case 2: return launch_static_np<DT, 2, WIDE>(c, info);
+    case 3: return launch_static_np<DT, 3, WIDE>(c, info);
+    case 4: return launch_static_np<DT, 4, WIDE>(c, info);
+    case 5: return launch_static_np<DT, 5, WIDE>(c, info);
+    case 6: return launch_static_np<DT, 6, WIDE>(c, info);
+    case 7: return launch_static_np<DT, 7, WIDE>(c, info);
+    case 8: return launch_static_np<DT, 8, WIDE>(c, info);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -215,11 +215,23 @@ typedef enum {
                                     SMs to kernels on other streams; 0 = no cap
                                     (default).  Below the SM count, ring / tree
                                     all-reduces and reduce-scatters with P <= 8
-                                    and at least 4 KiB per rank per block, and
+                                    run the kernel AR_OPT_CAPPED_KERNEL names,
+                                    one block per SM (the TMA pipeline needs at
+                                    least 4 KiB per rank per block, else the
+                                    256-thread load/store kernel runs), and
                                     all-gathers of whole 16-byte pieces with at
-                                    least 32 KiB per block, run TMA bulk-copy
-                                    pipelines, one block per SM.  Results do not
-                                    change.                                         */
+                                    least 32 KiB per block run a TMA bulk-copy
+                                    pipeline.  Results do not change.              */
+    AR_OPT_CAPPED_KERNEL = 9,    /* kernel that P <= 8 ring / tree all-reduces and
+                                    reduce-scatters run when AR_OPT_MAX_BLOCKS is
+                                    below the SM count: AR_CAPPED_WIDE (default;
+                                    1024-thread load/store blocks, one per SM --
+                                    measured fastest alone) or AR_CAPPED_TMA (the
+                                    TMA bulk-copy pipeline -- measured fastest
+                                    beside GEMMs on the other SMs).  The initial
+                                    value comes from the environment variable
+                                    AR_CAPPED_KERNEL=wide|tma at ar_init.  Results
+                                    do not change.                                 */
     AR_OPT_LL_EPOCH = 8          /* test hook: sets the last epoch used by LL and
                                     LL128 (0 .. 2^32 - 2; the next call uses
                                     value + 1; the call that uses 2^32 - 1 clears
@@ -227,6 +239,10 @@ typedef enum {
                                     device memory synchronously: synchronize the
                                     communicator's streams first.                 */
 } ar_option_t;
+
+/* Values of AR_OPT_CAPPED_KERNEL. */
+#define AR_CAPPED_WIDE 0
+#define AR_CAPPED_TMA 1
 
 ar_status_t ar_set_option(ar_comm_t comm, ar_option_t option, long long value);
 

@@ -175,3 +175,20 @@ def host_inputs(sends, kind: str, seed: int, sigma: float = 1.0, start: int = 0,
         if not np.array_equal(h[idx].view(np.uint8), cols[r].view(np.uint8)):
             raise AssertionError(f"rank {r}: device inputs differ from the host generator")
     return host
+
+
+def init_comm(P: int, capped_kernel: str | None = None) -> int:
+    """ar_init with AR_CAPPED_KERNEL set to `capped_kernel` ("wide" or "tma":
+    the kernel that P <= 8 all-reduces and reduce-scatters capped below the SM
+    count run) while the communicator is created; None leaves the default."""
+    if capped_kernel is None:
+        return ar.ar_init(P)
+    old = os.environ.get("AR_CAPPED_KERNEL")
+    os.environ["AR_CAPPED_KERNEL"] = capped_kernel
+    try:
+        return ar.ar_init(P)
+    finally:
+        if old is None:
+            os.environ.pop("AR_CAPPED_KERNEL", None)
+        else:
+            os.environ["AR_CAPPED_KERNEL"] = old

@@ -22,7 +22,7 @@ import torch
 import allreduce_reduction_emulated_gb300 as ar
 import oracle
 import pins
-from gpu_util import oracle_full, to_device, to_host
+from gpu_util import init_comm, oracle_full, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -97,11 +97,13 @@ def test_edges_every_algorithm(P, Q, dev):
         ar.ar_destroy(comm)
 
 
+@pytest.mark.parametrize("kind", ["wide", "tma"])
 @pytest.mark.parametrize("P", [4, 8])
-def test_edges_on_a_few_sms(P, dev):
-    """The TMA pipeline (8 SMs): its tiles are loaded rotated per ring chunk,
-    so a chunk edge inside a tile takes the per-element path."""
-    comm = ar.ar_init(P)
+def test_edges_on_a_few_sms(P, kind, dev):
+    """Capped to 8 SMs: the wide kernel, and the TMA pipeline, whose tiles are
+    loaded rotated per ring chunk, so a chunk edge inside a tile takes the
+    per-element path."""
+    comm = init_comm(P, kind)
     try:
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, 8)
         for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
@@ -147,15 +149,16 @@ def test_hierarchical_subchunk_edges(P, Q, dev):
         ar.ar_destroy(comm)
 
 
+@pytest.mark.parametrize("kind", ["wide", "tma"])
 @pytest.mark.parametrize("P", [4, 8, 12])
-def test_reduce_scatter_shard_edges(P, dev):
+def test_reduce_scatter_shard_edges(P, kind, dev):
     """Shard s is ring chunk s, folded from rank s: with the crafted data
     started at rank c, shards c+1..c+3 reduce to 2 and the others to 0, so a
     tile that crosses a shard edge and keeps the wrong order shows; every start
     rank runs, so every shard edge is a 0|2 step once.  Element-wise shards
-    (not whole vectors), whole-vector shards, and the TMA pipeline on 8 SMs
-    (P <= 8)."""
-    comm = ar.ar_init(P)
+    (not whole vectors), whole-vector shards, and 8 SMs (P <= 8: the wide
+    kernel or the TMA pipeline)."""
+    comm = init_comm(P, kind)
     try:
         for dtype in (ar.AR_FLOAT32, ar.AR_BFLOAT16):
             for rc, blocks in ((5, 0), (1003, 0), (1024, 0), (65536 + 8, 0), (65536 + 8, 8), (3 * 4096 + 8, 8)):

@@ -62,11 +62,19 @@ def test_finish_requires_every_bucket(recorder):
 
 
 def test_block_cap_set_before_each_bucket(recorder):
+    """The cap and the capped kernel (the TMA pipeline by default: measured
+    faster beside the gradient GEMMs) are set before every bucket."""
     red, _, _ = make(max_blocks=48)
     red.ready(1000, "e")
     kinds = [c[0] for c in recorder]
-    assert kinds == ["option", "allreduce"] * 4
-    assert all(c[1] == ar.AR_OPT_MAX_BLOCKS and c[2] == 48 for c in recorder if c[0] == "option")
+    assert kinds == ["option", "option", "allreduce"] * 4
+    opts = [c for c in recorder if c[0] == "option"]
+    assert opts[0::2] == [("option", ar.AR_OPT_MAX_BLOCKS, 48)] * 4
+    assert opts[1::2] == [("option", ar.AR_OPT_CAPPED_KERNEL, ar.AR_CAPPED_TMA)] * 4
+    recorder.clear()
+    red, _, _ = make(max_blocks=48, capped_kernel=ar.AR_CAPPED_WIDE)
+    red.ready(1000, "e")
+    assert [c for c in recorder if c[0] == "option"][1] == ("option", ar.AR_OPT_CAPPED_KERNEL, ar.AR_CAPPED_WIDE)
 
 
 def test_no_cap_leaves_the_option_alone(recorder):
@@ -91,7 +99,7 @@ def test_auto_cap_is_the_measured_share_of_the_sms(recorder, monkeypatch):
     red, _, _ = make(max_blocks="auto")
     assert red.max_blocks == 48
     red.ready(1000, "e")
-    assert all(c[2] == 48 for c in recorder if c[0] == "option")
+    assert all(c[2] == 48 for c in recorder if c[0] == "option" and c[1] == ar.AR_OPT_MAX_BLOCKS)
     Props.multi_processor_count = 132
     assert B.auto_max_blocks("cuda:0") == 42
     Props.multi_processor_count = 1

@@ -1,13 +1,14 @@
-"""The TMA bulk-copy all-reduce, reduce-scatter (P <= 8) and all-gather (any
-P), capped to fewer SMs than the GPU has, against the oracle, bit for bit.
+"""Collectives capped to fewer SMs than the GPU has, against the oracle, bit
+for bit: the all-reduce and reduce-scatter (P <= 8) in both capped kernels --
+the wide load/store shape (1024-thread blocks, the default) and the TMA
+bulk-copy pipeline (AR_CAPPED_KERNEL=tma) -- and the TMA all-gather (any P).
 
 "NCCL, NIXL, and Distributed GPU Communication" (the overlap checklist): the
-all-reduce runs beside computation, so AR_OPT_MAX_BLOCKS gives it a few SMs;
-below the SM count the rank-specialised ring / tree fold runs as a pipeline of
-bulk copies through shared memory.  Same orders as the uncapped kernel, so the
-two agree element for element; ragged counts exercise partial tiles and the
-trailing partial vector; the bounded mbarrier waits are made to run out with
-the producer-skip test hook.
+all-reduce runs beside computation, so AR_OPT_MAX_BLOCKS gives it a few SMs.
+Same orders as the uncapped kernel, so the results agree element for element;
+ragged counts exercise partial tiles and the trailing partial vector; the TMA
+pipeline's bounded mbarrier waits are made to run out with the producer-skip
+test hook.
 """
 import numpy as np
 import pytest
@@ -16,13 +17,14 @@ import torch
 import allreduce_reduction_emulated_gb300 as ar
 import oracle
 import pins
-from gpu_util import (VEC, Guarded, assert_equal_every_element, device_inputs, host_inputs, oracle_full,
-                      to_device, to_host)
+from gpu_util import (VEC, Guarded, assert_equal_every_element, device_inputs, host_inputs, init_comm,
+                      oracle_full, to_device, to_host)
 
 pytestmark = pytest.mark.gpu
 
 OPS = (ar.AR_SUM, ar.AR_MIN, ar.AR_MAX)
 BLOCKS = 16
+KINDS = ("wide", "tma")   # AR_CAPPED_KERNEL: the capped all-reduce / reduce-scatter kernel
 
 
 @pytest.fixture(scope="module")
@@ -41,11 +43,12 @@ def tma_counts(dtype):
     return [BLOCKS * tile, BLOCKS * tile + 3 * V + 1, 37 * tile + V - 1, 200_003]
 
 
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("P", [1, 2, 3, 5, 8])
 @pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
-def test_capped_calls_match_the_oracle(P, dtype, dev, capfd):
+def test_capped_calls_match_the_oracle(P, dtype, kind, dev, capfd):
     rng = np.random.default_rng(800 + 10 * P + dtype)
-    comm = ar.ar_init(P)
+    comm = init_comm(P, kind)
     try:
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
         ar.ar_set_option(comm, ar.AR_OPT_DEBUG, 1)
@@ -65,17 +68,18 @@ def test_capped_calls_match_the_oracle(P, dtype, dev, capfd):
                         pins.assert_bitwise(to_host(outs[r].tensor), want[r],
                                             f"P={P} dtype={dtype} count={count} op={op} algo={algo} rank={r}")
         log = capfd.readouterr().err
-        assert "kernel=tma_ring" in log and "kernel=tma_tree" in log
+        assert f"kernel={kind}_ring" in log and f"kernel={kind}_tree" in log
     finally:
         ar.ar_destroy(comm)
 
 
-def test_full_size_equals_the_uncapped_kernel(dev):
+@pytest.mark.parametrize("kind", KINDS)
+def test_full_size_equals_the_uncapped_kernel(kind, dev):
     """8 x 64 MiB fp32, ring, scale 1/8 on 64 SMs: every element against the
     oracle, and element for element the uncapped kernel's result, in place
     and out of place."""
     P, count = 8, 16 * 1024 * 1024
-    comm = ar.ar_init(P)
+    comm = init_comm(P, kind)
     try:
         sends = device_inputs("normal", 0, P, count, dev, 1e-3)
         ref = [torch.empty_like(s) for s in sends]
@@ -99,8 +103,9 @@ def test_full_size_equals_the_uncapped_kernel(dev):
 
 
 def test_bounded_waits_report_a_timeout_and_recover(dev):
+    """The TMA pipeline's mbarrier waits (the wide kernel has none)."""
     P, count = 8, 1 << 20
-    comm = ar.ar_init(P)
+    comm = init_comm(P, "tma")
     try:
         rng = np.random.default_rng(12)
         sends = pins.random_inputs(rng, P, count, ar.AR_FLOAT32)
@@ -124,14 +129,15 @@ def test_bounded_waits_report_a_timeout_and_recover(dev):
         ar.ar_destroy(comm)
 
 
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("P", [1, 2, 3, 8])
 @pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
-def test_capped_reduce_scatter_matches_the_oracle(P, dtype, dev, capfd):
+def test_capped_reduce_scatter_matches_the_oracle(P, dtype, kind, dev, capfd):
     """Reduce-scatter on 16 SMs: shard s folded in ring chunk s's order, stored
     to its owner only; shards of whole 4 KiB tiles and shards whose edges fall
-    inside a tile (stored segment by segment)."""
+    inside a tile (the TMA pipeline stores those segment by segment)."""
     rng = np.random.default_rng(900 + 10 * P + dtype)
-    comm = ar.ar_init(P)
+    comm = init_comm(P, kind)
     used = False
     try:
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
@@ -150,15 +156,16 @@ def test_capped_reduce_scatter_matches_the_oracle(P, dtype, dev, capfd):
                     assert outs[r].guards_intact()
                     pins.assert_bitwise(to_host(outs[r].tensor), want[r],
                                         f"RS P={P} dtype={dtype} rc={rc} op={op} rank={r}")
-        used = "kernel=tma_reduce_scatter" in capfd.readouterr().err
+        used = f"kernel={kind}_reduce_scatter" in capfd.readouterr().err
     finally:
         ar.ar_destroy(comm)
     assert used
 
 
-def test_capped_reduce_scatter_in_place(dev):
+@pytest.mark.parametrize("kind", KINDS)
+def test_capped_reduce_scatter_in_place(kind, dev):
     P, rc = 8, 20000
-    comm = ar.ar_init(P)
+    comm = init_comm(P, kind)
     try:
         ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
         rng = np.random.default_rng(31)
@@ -269,7 +276,7 @@ print("ok")
 
 
 def test_first_capped_call_inside_a_graph_capture(dev):
-    """The kernel's shared-memory opt-in happens on a device's first capped
+    """The TMA kernel's shared-memory opt-in happens on a device's first capped
     call; here that call is being captured (in a fresh process)."""
     import os
     import subprocess
@@ -277,16 +284,18 @@ def test_first_capped_call_inside_a_graph_capture(dev):
 
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     out = subprocess.run([sys.executable, "-c", FIRST_CALL_CAPTURED.format(root=root)],
-                         capture_output=True, text=True, timeout=300)
+                         capture_output=True, text=True, timeout=300,
+                         env={**os.environ, "AR_CAPPED_KERNEL": "tma"})
     assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
 
 
-def test_full_size_reduce_scatter_and_all_gather_on_64_sms(dev):
-    """P=8, 8 MiB shards / pieces (the bench's sizes): the capped TMA kernels
+@pytest.mark.parametrize("kind", KINDS)
+def test_full_size_reduce_scatter_and_all_gather_on_64_sms(kind, dev):
+    """P=8, 8 MiB shards / pieces (the bench's sizes): the capped kernels
     equal the uncapped kernels element for element, and every reduce-scatter
     output element equals the oracle's."""
     P, rc = 8, 2 * 1024 * 1024
-    comm = ar.ar_init(P)
+    comm = init_comm(P, kind)
     try:
         sends = device_inputs("normal", 0, P, P * rc, dev, 1e-3)
         ref = [torch.empty(rc, device=dev) for _ in range(P)]
@@ -308,5 +317,33 @@ def test_full_size_reduce_scatter_and_all_gather_on_64_sms(dev):
         for s in range(P):
             assert_equal_every_element(got[s], want[s], f"capped reduce-scatter shard {s}")
         assert_equal_every_element(gathered[0], np.concatenate(want), "all-gather of the shards, rank 0")
+    finally:
+        ar.ar_destroy(comm)
+
+
+def test_capped_kernel_option(dev, capfd):
+    """AR_OPT_CAPPED_KERNEL switches the capped kernel at run time; other
+    values are refused; uncapped calls are unaffected."""
+    P, count = 8, 1 << 18
+    comm = ar.ar_init(P)
+    try:
+        rng = np.random.default_rng(61)
+        sends = pins.random_inputs(rng, P, count, ar.AR_FLOAT32)
+        xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+        want = oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.RING)
+        with pytest.raises(ar.ArError) as e:
+            ar.ar_set_option(comm, ar.AR_OPT_CAPPED_KERNEL, 2)
+        assert e.value.status == ar.AR_ERR_INVALID_ARG
+        ar.ar_set_option(comm, ar.AR_OPT_DEBUG, 1)
+        for blocks, kind, kernel in ((16, ar.AR_CAPPED_TMA, "tma_ring"), (16, ar.AR_CAPPED_WIDE, "wide_ring"),
+                                     (0, ar.AR_CAPPED_TMA, "static_ring")):
+            ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, blocks)
+            ar.ar_set_option(comm, ar.AR_OPT_CAPPED_KERNEL, kind)
+            ys = [torch.empty_like(x) for x in xs]
+            ar.ar_allreduce(comm, xs, ys, count, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_RING, 1.0)
+            torch.cuda.synchronize()
+            assert f"kernel={kernel} " in capfd.readouterr().err
+            pins.assert_bitwise(to_host(ys[2]), want[2], f"{kernel}")
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
     finally:
         ar.ar_destroy(comm)
