@@ -223,11 +223,21 @@ cudaError_t launch_ll_one(const Call& c, LaunchInfo* info) {
   p.skip_produce = c.skip_produce;
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   p.scale = c.scale;
-  // one staged word per thread for P <= 8 (slices of 256 / P words, at least 32)
-  int slice = kLLThreads / (c.P < 1 ? 1 : c.P);
-  if (slice < kLLMinSlice) slice = kLLMinSlice;
-  p.slice_words = slice;
-  const uint64_t grid = (p.nwords + (uint64_t)slice - 1) / (uint64_t)slice;
+  // one staged word per thread for P <= 8 (slices of 256 / P words, at least
+  // 32), widened so that the grid fits in one wave of resident blocks
+  static const int blocks_per_sm = [&] {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kLLBlock, 0) != cudaSuccess) b = 1;
+    return b > 0 ? b : 1;
+  }();
+  const uint64_t wave = (uint64_t)blocks_per_sm * (uint64_t)(c.sms > 0 ? c.sms : 1);
+  uint64_t slice = (uint64_t)(kLLThreads / (c.P < 1 ? 1 : c.P));
+  if (slice < (uint64_t)kLLMinSlice) slice = kLLMinSlice;
+  const uint64_t per_wave = (p.nwords + wave - 1) / wave;
+  if (slice < per_wave) slice = per_wave;
+  if (slice > 0x7fffffffull) return cudaErrorInvalidValue;
+  p.slice_words = (int)slice;
+  const uint64_t grid = (p.nwords + slice - 1) / slice;
   if (grid == 0 || grid > 0x7fffffffull) return cudaErrorInvalidValue;
   kernel<<<(unsigned)grid, kLLBlock, 0, c.stream>>>(p);
   const cudaError_t e = cudaGetLastError();

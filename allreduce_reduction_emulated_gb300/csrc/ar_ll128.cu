@@ -259,11 +259,22 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   p.scale = c.scale;
   if (p.nlines * kLineWords > p.stride) return cudaErrorInvalidValue;
-  // the 8 warps stage 32 lines at once: 4 lines of each of 8 ranks, more for fewer ranks
-  int slice = kRoundLines / (c.P < 1 ? 1 : c.P);
-  if (slice < kWarpLines) slice = kWarpLines;
-  p.slice_lines = slice;
-  const uint64_t grid = (p.nlines + (uint64_t)slice - 1) / (uint64_t)slice;
+  // the 8 warps stage 32 lines at once: 4 lines of each of 8 ranks, more for
+  // fewer ranks; slices widened so that the grid fits in one wave of resident
+  // blocks (a second, nearly empty wave doubled the time at 512 KiB per rank)
+  static const int blocks_per_sm = [&] {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kBlock, 0) != cudaSuccess) b = 1;
+    return b > 0 ? b : 1;
+  }();
+  const uint64_t wave = (uint64_t)blocks_per_sm * (uint64_t)(c.sms > 0 ? c.sms : 1);
+  uint64_t slice = (uint64_t)(kRoundLines / (c.P < 1 ? 1 : c.P));
+  if (slice < (uint64_t)kWarpLines) slice = kWarpLines;
+  const uint64_t per_wave = (p.nlines + wave - 1) / wave;
+  if (slice < per_wave) slice = per_wave;
+  if (slice > 0x7fffffffull) return cudaErrorInvalidValue;
+  p.slice_lines = (int)slice;
+  const uint64_t grid = (p.nlines + slice - 1) / slice;
   if (grid == 0 || grid > 0x7fffffffull) return cudaErrorInvalidValue;
   kernel<<<(unsigned)grid, kBlock, 0, c.stream>>>(p);
   const cudaError_t e = cudaGetLastError();

@@ -53,8 +53,8 @@ PROFILES = {
     "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll128.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32": ("static_reduce_scatter_p8_8MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
-    "p8_64MiB_fp32_ring_ddp_mean_64sm": ("tma_ring_p8_64MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_f32.cu"], 1.0),
-    "p8_rs_8MiB_shards_fp32_64sm": ("tma_reduce_scatter_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_f32.cu"], 1.0),
+    "p8_64MiB_fp32_ring_ddp_mean_64sm": ("wide_ring_p8_64MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_wide_f32.cu"], 1.0),
+    "p8_rs_8MiB_shards_fp32_64sm": ("wide_reduce_scatter_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_wide_f32.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32_64sm": ("tma_all_gather_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_gather.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32": ("all_gather_p8_8MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_collectives.cu"], 1.0),
 }
@@ -96,12 +96,12 @@ WORKLOADS = {
                                    op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter"),
     "p8_ag_8MiB_shards_fp32": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                    op="sum", algo="ring", scale=1.0, seed=0, coll="all_gather"),
-    # the headline on 64 of the 152 SMs (AR_OPT_MAX_BLOCKS): the TMA bulk-copy pipeline, for
-    # an all-reduce that shares the GPU with computation
+    # the headline on 64 of the 152 SMs (AR_OPT_MAX_BLOCKS): the wide kernel (1024-thread
+    # blocks, one per SM), for an all-reduce that shares the GPU with computation
     "p8_64MiB_fp32_ring_ddp_mean_64sm": dict(P=8, count=16 * 1024 * 1024, kind="normal", sigma=1e-3,
                                              dtype="f32", op="sum", algo="ring", scale=0.125, seed=0,
                                              max_blocks=64),
-    # the reduce-scatter on 64 SMs (TMA pipeline): gradient shards beside computation
+    # the reduce-scatter on 64 SMs (the wide kernel): gradient shards beside computation
     "p8_rs_8MiB_shards_fp32_64sm": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                         op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter",
                                         max_blocks=64),
