@@ -32,17 +32,25 @@ __device__ __forceinline__ uint32_t ll_epoch_begin(const unsigned int* state) {
   return s_epoch;
 }
 
-// Called by ONE thread of each block, any time after ll_epoch_begin (the
-// barrier there orders the block's read of state[0] before this thread's
-// fence).  The block that completes the count publishes the epoch at once:
-// every block has read the old value by then, and the next call starts only
-// after this kernel ends, so the publication need not wait for the other
-// blocks to finish.  The wrap epoch is counted in ll_epoch_end instead.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(unsigned int* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Called by ONE thread of each block, any time after ll_epoch_begin.  The
+// count-in is one acquire-release read-modify-write: its release half orders
+// the block's read of state[0] (made before the barrier in ll_epoch_begin,
+// which this thread has passed) before the increment, and the block that
+// completes the count acquires every earlier increment, so all blocks' reads
+// happen before its publication of the epoch, which follows in program order.
+// (A full fence before a relaxed add gives the same order and measured about
+// 0.6 us longer per call.)  The publication need not wait for the other blocks
+// to finish: every block has read the old value, and the next call starts only
+// after this kernel ends.  The wrap epoch is counted in ll_epoch_end instead.
 __device__ __forceinline__ void ll_epoch_arrive(unsigned int* state, uint32_t epoch) {
   if (epoch == kLLEpochWrap) return;
-  __threadfence();
-  if (atomicAdd(&state[1], 1u) == gridDim.x - 1) {
-    __threadfence();
+  if (atom_add_acq_rel_u32(&state[1], 1u) == gridDim.x - 1) {
     st_relaxed_u32(&state[1], 0u);
     st_relaxed_u32(&state[0], epoch);
   }

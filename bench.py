@@ -46,6 +46,9 @@ PROFILES = {
     "p72_4MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
     "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll.cu"], 1.0),
+    "p8_64KiB_fp32_ll": ("ll_p8_64KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll.cu"], 1.0),
+    "p8_4KiB_fp32_ring": ("static_ring_p8_4KiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
+    "p8_64KiB_fp32_ring": ("static_ring_p8_64KiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_4MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
     "p72_16MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
@@ -91,6 +94,14 @@ WORKLOADS = {
                                  algo="ll128", scale=1.0, seed=0),
     "p8_4KiB_fp32_ll": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
                             algo="ll", scale=1.0, seed=0),
+    # small messages for per-launch kernel times (ncu's gpu__time_duration resolves what the
+    # ~2 us launch cadence of back-to-back small kernels hides): LL against the ring
+    "p8_4KiB_fp32_ring": dict(P=8, count=1024, kind="uniform", sigma=1.0, dtype="f32", op="sum",
+                              algo="ring", scale=1.0, seed=0),
+    "p8_64KiB_fp32_ll": dict(P=8, count=16384, kind="uniform", sigma=1.0, dtype="f32", op="sum",
+                             algo="ll", scale=1.0, seed=0),
+    "p8_64KiB_fp32_ring": dict(P=8, count=16384, kind="uniform", sigma=1.0, dtype="f32", op="sum",
+                               algo="ring", scale=1.0, seed=0),
     # the ring's two halves as standalone collectives: count = elements per shard
     "p8_rs_8MiB_shards_fp32": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                    op="sum", algo="ring", scale=0.125, seed=0, coll="reduce_scatter"),
