@@ -121,3 +121,50 @@ def test_ll128_bounded_wait_limit_and_capture(dev):
                                 "LL128 call replayed from the capture")
     finally:
         ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P", [2, 8, 13])
+def test_ll_at_its_largest_limit(P, dev):
+    """LL with its limit raised to the 1 MiB maximum (AR_LL_MAX_BYTES at
+    ar_init): past about 32 words per block per resident wave the slices
+    widen beyond one word per thread, so threads stage and receive several
+    words each.  Every element against the oracle's ring order, the epoch
+    wrap included."""
+    import os
+
+    old = os.environ.get("AR_LL_MAX_BYTES")
+    os.environ["AR_LL_MAX_BYTES"] = str(1 << 20)
+    try:
+        comm = ar.ar_init(P)
+    finally:
+        if old is None:
+            os.environ.pop("AR_LL_MAX_BYTES", None)
+        else:
+            os.environ["AR_LL_MAX_BYTES"] = old
+    try:
+        rng = np.random.default_rng(1300 + P)
+        cases = [(ar.AR_FLOAT32, 262144, 0.125), (ar.AR_FLOAT32, 200_003, 1.0), (ar.AR_BFLOAT16, 524287, 1.0),
+                 (ar.AR_INT32, 150_001, 1.0)]
+        for dtype, count, scale in cases:
+            sends = pins.random_inputs(rng, P, count, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            outs = [Guarded(count, dtype, dev) for _ in range(P)]
+            ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, dtype, ar.AR_SUM, ar.AR_ALGO_LL, scale)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            want = oracle.allreduce(sends, dtype, oracle.SUM, oracle.LL, scale)
+            for r in (0, P - 1):
+                assert outs[r].guards_intact()
+                pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"LL 1 MiB P={P} dtype={dtype} count={count} rank={r}")
+        ar.ar_set_option(comm, ar.AR_OPT_LL_EPOCH, 2**32 - 3)       # across the wrap at this size
+        for i in range(4):
+            sends = pins.random_inputs(rng, P, 262144, ar.AR_FLOAT32)
+            xs = [to_device(a, ar.AR_FLOAT32, dev) for a in sends]
+            ys = [torch.empty_like(x) for x in xs]
+            ar.ar_allreduce(comm, xs, ys, 262144, ar.AR_FLOAT32, ar.AR_SUM, ar.AR_ALGO_LL, 1.0)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            want = oracle.allreduce(sends, ar.AR_FLOAT32, oracle.SUM, oracle.LL)
+            pins.assert_bitwise(to_host(ys[1 % P]), want[1 % P], f"LL 1 MiB wrap call {i}")
+    finally:
+        ar.ar_destroy(comm)
