@@ -347,3 +347,46 @@ def test_capped_kernel_option(dev, capfd):
         assert ar.ar_get_status(comm) == ar.AR_SUCCESS
     finally:
         ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("P", [1, 3, 8])
+@pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
+def test_capped_small_messages(P, dtype, kind, dev):
+    """Capped calls on messages too small to give every block a tile: the
+    wide kernel takes them (one partial block and the trailing partial
+    vector), or with AR_CAPPED_TMA the 256-thread kernel does; every output
+    element against the oracle."""
+    rng = np.random.default_rng(1700 + 10 * P + dtype)
+    comm = init_comm(P, kind)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        V = VEC[dtype]
+        for count in (1, 2, V - 1, V + 1, 33, 1000, 4099, 1024 * V + 5):
+            sends = pins.random_inputs(rng, P, count, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            for op in OPS:
+                for algo, oalgo in ((ar.AR_ALGO_RING, oracle.RING), (ar.AR_ALGO_TREE, oracle.TREE)):
+                    scale = 0.125 if (op == ar.AR_SUM and dtype != ar.AR_INT32) else 1.0
+                    outs = [Guarded(count, dtype, dev) for _ in range(P)]
+                    ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, dtype, op, algo, scale)
+                    torch.cuda.synchronize()
+                    assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                    want = oracle.allreduce(sends, dtype, op, oalgo, scale)
+                    for r in range(P):
+                        assert outs[r].guards_intact()
+                        pins.assert_bitwise(to_host(outs[r].tensor), want[r],
+                                            f"{kind} P={P} dtype={dtype} count={count} op={op} algo={algo} rank={r}")
+        for rc in (V, 3 * V, 100 * V, 1025 * V):              # whole-vector shards: the capped kernels
+            sends = pins.random_inputs(rng, P, P * rc, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            outs = [Guarded(rc, dtype, dev) for _ in range(P)]
+            ar.ar_reduce_scatter(comm, xs, [o.tensor for o in outs], rc, dtype, ar.AR_MAX, 1.0)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            want = oracle.reduce_scatter(sends, dtype, oracle.MAX, 1.0)
+            for r in range(P):
+                assert outs[r].guards_intact()
+                pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"{kind} RS P={P} dtype={dtype} rc={rc} rank={r}")
+    finally:
+        ar.ar_destroy(comm)
