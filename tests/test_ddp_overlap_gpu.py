@@ -31,10 +31,12 @@ def dev():
 
 
 @pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
-@pytest.mark.parametrize("max_blocks", [None, 16, "auto"])
-def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks, gdt):
+@pytest.mark.parametrize("max_blocks,capped", [(None, None), (16, None), ("auto", None), (16, ar.AR_CAPPED_WIDE)],
+                         ids=["uncapped", "16", "auto", "16-wide"])
+def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks, capped, gdt):
     """max_blocks=16 or "auto" (48 of 152 SMs): the bucket all-reduces run on a
-    few SMs (the TMA pipeline).
+    few SMs (the TMA pipeline, BucketReducer's default beside computation, or
+    the wide load/store kernel).
     bf16: bf16 GEMMs write bf16 gradients, reduced with fp32 accumulation."""
     P, T, bucket = 4, 96, 300_000
     shapes = [(512, 1024), (1024, 512), (512, 768)] * 2          # 6 "parameters", backward order
@@ -48,7 +50,8 @@ def test_overlapped_buckets_match_serial_and_oracle(dev, max_blocks, gdt):
             grads = [torch.zeros(total, dtype=gdt, device=dev) for _ in range(P)]
             outs = [torch.full((total,), float("nan"), dtype=gdt, device=dev) for _ in range(P)]
             compute = torch.cuda.Stream()
-            red = BucketReducer(comm, grads, bucket, scale=0.25, out=outs, max_blocks=max_blocks)
+            kw = {} if capped is None else {"capped_kernel": capped}
+            red = BucketReducer(comm, grads, bucket, scale=0.25, out=outs, max_blocks=max_blocks, **kw)
             torch.cuda.synchronize()              # buffers initialised on the default stream
             with torch.cuda.stream(compute):
                 off = 0
