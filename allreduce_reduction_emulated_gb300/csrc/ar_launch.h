@@ -77,6 +77,11 @@ constexpr size_t kTmaTileBytes = 4096;
 cudaError_t launch_all_gather_tma(const Call& c, LaunchInfo* info);
 constexpr size_t kTmaGatherTileBytes = 32768;
 cudaError_t launch_generic(const Call& c, LaunchInfo* info);
+// the same pipelined kernels in 768-thread blocks, at most one per SM (calls
+// capped below the SM count; launch_generic and launch_reduce_scatter_vec
+// forward to them)
+cudaError_t launch_generic_wide(const Call& c, LaunchInfo* info);
+cudaError_t launch_reduce_scatter_vec_wide(const Call& c, LaunchInfo* info);
 cudaError_t launch_ll(const Call& c, LaunchInfo* info);
 // LL128: 128-byte lines of 120 payload bytes + a flag word (staging, stage_stride)
 cudaError_t launch_ll128(const Call& c, LaunchInfo* info);

@@ -35,27 +35,30 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 _CSRC = "allreduce_reduction_emulated_gb300/csrc/"
 _STATIC = [_CSRC + "ar_device.cuh", _CSRC + "ar_static.cuh"]
+_GENERIC = [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cuh", _CSRC + "ar_generic.cu"]
+_GENERIC_WIDE = [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cuh", _CSRC + "ar_generic_wide.cu"]
 # per workload: (ncu summary under profiles/, kernel sources it was taken on,
 #                launches of the profiled case per launch of this workload)
 PROFILES = {
     "p8_64MiB_fp32_ring_ddp_mean": ("static_ring_p8_64MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p8_64MiB_bf16_tree": ("static_tree_p8_64MiB_bf16.ncu.txt", _STATIC + [_CSRC + "ar_static_bf16.cu"], 1.0),
     "p8_256MiB_bf16_tree": ("static_tree_p8_64MiB_bf16.ncu.txt", _STATIC + [_CSRC + "ar_static_bf16.cu"], 4.0),
-    "p72_4MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
-    "p72_16MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
-    "p72_4MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
-    "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
+    "p72_4MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", _GENERIC, 1.0),
+    "p72_16MiB_int32_sum_ring": ("pipelined_ring_p72_4MiB_int32.ncu.txt", _GENERIC, 4.0),
+    "p72_4MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", _GENERIC, 1.0),
+    "p72_16MiB_int32_max_tree": ("pipelined_tree_p72_4MiB_int32.ncu.txt", _GENERIC, 4.0),
     "p8_4KiB_fp32_ll": ("ll_p8_4KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll.cu"], 1.0),
     "p8_64KiB_fp32_ll": ("ll_p8_64KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll.cu"], 1.0),
     "p8_4KiB_fp32_ring": ("static_ring_p8_4KiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
     "p8_64KiB_fp32_ring": ("static_ring_p8_64KiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
-    "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
-    "p72_4MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
-    "p72_16MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
-    "p72_16MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 4.0),
+    "p72_4MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", _GENERIC, 1.0),
+    "p72_4MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", _GENERIC, 1.0),
+    "p72_16MiB_int32_sum_hier": ("pipelined_hier_p72_4MiB_int32.ncu.txt", _GENERIC, 4.0),
+    "p72_16MiB_fp32_sum_hier": ("pipelined_hier_p72_4MiB_fp32.ncu.txt", _GENERIC, 4.0),
     "p8_512KiB_fp32_ll128": ("ll128_p8_512KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_ll_epoch.cuh", _CSRC + "ar_ll128.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32": ("static_reduce_scatter_p8_8MiB_fp32.ncu.txt", _STATIC + [_CSRC + "ar_static_f32.cu"], 1.0),
-    "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", [_CSRC + "ar_device.cuh", _CSRC + "ar_generic.cu"], 1.0),
+    "p72_rs_256KiB_shards_fp32": ("pipelined_reduce_scatter_p72_256KiB_fp32.ncu.txt", _GENERIC, 1.0),
+    "p72_16MiB_int32_sum_ring_64sm": ("wide_pipelined_ring_p72_16MiB_int32_64sm.ncu.txt", _GENERIC_WIDE, 1.0),
     "p8_64MiB_fp32_ring_ddp_mean_64sm": ("wide_ring_p8_64MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_wide_f32.cu"], 1.0),
     "p8_rs_8MiB_shards_fp32_64sm": ("wide_reduce_scatter_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_wide_f32.cu"], 1.0),
     "p8_ag_8MiB_shards_fp32_64sm": ("tma_all_gather_p8_8MiB_fp32_64sm.ncu.txt", _STATIC + [_CSRC + "ar_tma.cuh", _CSRC + "ar_tma_gather.cu"], 1.0),
@@ -120,6 +123,9 @@ WORKLOADS = {
     "p8_ag_8MiB_shards_fp32_64sm": dict(P=8, count=2 * 1024 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                         op="sum", algo="ring", scale=1.0, seed=0, coll="all_gather",
                                         max_blocks=64),
+    # config 5b's ring on 64 of the 152 SMs: the pipelined kernel in 768-thread blocks
+    "p72_16MiB_int32_sum_ring_64sm": dict(P=72, count=4 * 1024 * 1024, kind="int", sigma=1.0,
+                                          dtype="i32", op="sum", algo="ring", scale=1.0, seed=0, max_blocks=64),
     # reduce-scatter above the rank-specialised limit: 72 shards of 256 KiB (18 MiB per rank)
     "p72_rs_256KiB_shards_fp32": dict(P=72, count=64 * 1024, kind="normal", sigma=1e-3, dtype="f32",
                                       op="sum", algo="ring", scale=1.0 / 72, seed=0, coll="reduce_scatter"),

@@ -218,10 +218,12 @@ typedef enum {
                                     run the kernel AR_OPT_CAPPED_KERNEL names,
                                     one block per SM (the TMA pipeline needs at
                                     least 4 KiB per rank per block, else the
-                                    256-thread load/store kernel runs), and
-                                    all-gathers of whole 16-byte pieces with at
-                                    least 32 KiB per block run a TMA bulk-copy
-                                    pipeline.  Results do not change.              */
+                                    256-thread load/store kernel runs); more
+                                    ranks, and the hierarchical order, run the
+                                    pipelined kernel in 768-thread blocks, one
+                                    per SM; all-gathers of whole 16-byte pieces
+                                    with at least 32 KiB per block run a TMA
+                                    bulk-copy pipeline.  Results do not change.    */
     AR_OPT_CAPPED_KERNEL = 9,    /* kernel that P <= 8 ring / tree all-reduces and
                                     reduce-scatters run when AR_OPT_MAX_BLOCKS is
                                     below the SM count: AR_CAPPED_WIDE (default;

@@ -390,3 +390,51 @@ def test_capped_small_messages(P, dtype, kind, dev):
                 pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"{kind} RS P={P} dtype={dtype} rc={rc} rank={r}")
     finally:
         ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P,Q", [(9, 3), (13, 13), (72, 8)])
+@pytest.mark.parametrize("dtype", [ar.AR_FLOAT32, ar.AR_BFLOAT16, ar.AR_INT32])
+def test_capped_many_ranks(P, Q, dtype, dev, capfd):
+    """More than 8 ranks on 16 SMs: the pipelined kernel in 768-thread blocks
+    (one per SM, grid-stride) for the ring, tree and hierarchical orders and
+    the reduce-scatter; every output element against the oracle."""
+    rng = np.random.default_rng(1900 + P + dtype)
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, Q)
+        ar.ar_set_option(comm, ar.AR_OPT_DEBUG, 1)
+        V = VEC[dtype]
+        for count in (1, V + 3, 1000, BLOCKS * 768 * V + 2 * V + 1, 3 * BLOCKS * 768 * V - 5):
+            sends = pins.random_inputs(rng, P, count, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            for op in (ar.AR_SUM, ar.AR_MAX):
+                for algo in (ar.AR_ALGO_RING, ar.AR_ALGO_TREE, ar.AR_ALGO_HIER):
+                    outs = [Guarded(count, dtype, dev) for _ in range(P)]
+                    ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, dtype, op, algo, 1.0)
+                    torch.cuda.synchronize()
+                    assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+                    if algo == ar.AR_ALGO_HIER:
+                        want = oracle.allreduce_hier(sends, Q, dtype, op)
+                    else:
+                        want = oracle.allreduce(sends, dtype, op, oracle.TREE if algo == ar.AR_ALGO_TREE else oracle.RING)
+                    for r in (0, P - 1):
+                        assert outs[r].guards_intact()
+                        pins.assert_bitwise(to_host(outs[r].tensor), want[r],
+                                            f"P={P} dtype={dtype} count={count} op={op} algo={algo} rank={r}")
+        for rc in (V, 200 * V, BLOCKS * 768 * V // P + V):
+            sends = pins.random_inputs(rng, P, P * rc, dtype)
+            xs = [to_device(a, dtype, dev) for a in sends]
+            outs = [Guarded(rc, dtype, dev) for _ in range(P)]
+            ar.ar_reduce_scatter(comm, xs, [o.tensor for o in outs], rc, dtype, ar.AR_SUM, 1.0)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            want = oracle.reduce_scatter(sends, dtype, oracle.SUM, 1.0)
+            for r in range(P):
+                assert outs[r].guards_intact()
+                pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"RS P={P} dtype={dtype} rc={rc} rank={r}")
+        log = capfd.readouterr().err
+        for k in ("wide_pipelined_ring", "wide_pipelined_tree", "wide_pipelined_hier", "wide_pipelined_reduce_scatter"):
+            assert f"kernel={k} " in log, k
+    finally:
+        ar.ar_destroy(comm)
