@@ -196,8 +196,42 @@ struct RankCursor {
   }
 };
 
+// The cursor of column v, and (ring) its chunk index = the chunk's start rank.
+template <int DT, int ALGO>
+__device__ __forceinline__ RankCursor<ALGO> column_cursor(const GenericParams& p, uint64_t v,
+                                                          const int16_t (*s_push)[AR_MAX_RANKS], int& first) {
+  RankCursor<ALGO> cur;
+  cur.P = p.P;
+  first = ALGO == kRing ? (int)(v / p.split) : 0;
+  if constexpr (ALGO == kRing) {
+    cur.a = first;
+  } else if constexpr (ALGO == kTree) {
+    cur.push = s_push[v >= p.split ? 1 : 0];
+    cur.a = 0;
+  } else {
+    // hierarchical: intra-group chunk c1 (split = its length in vectors), then
+    // sub-chunk c2 of that chunk across the G groups
+    const uint64_t V = 16 / Lanes<DT>::kBytes;
+    const uint64_t c1 = v / p.split;
+    const uint64_t lo = c1 * p.split * V;
+    const uint64_t hi = lo + p.split * V < p.count ? lo + p.split * V : p.count;
+    const int G = p.P / p.Q;
+    const uint64_t L2v = ((hi - lo + G - 1) / G + V - 1) / V;
+    const uint64_t c2 = (v - c1 * p.split) / L2v;
+    cur.Q = p.Q;
+    cur.G = G;
+    cur.a0 = cur.a = (int)(c1 % (uint64_t)p.Q);
+    cur.b0 = cur.b = (int)c2;
+  }
+  return cur;
+}
+
 // SCATTER (ring only): reduce-scatter -- chunk c is shard c and its result
 // goes only to rank c's receive buffer, at the shard-relative position.
+// Under a cap a thread walks several columns (grid-stride); the first W
+// copies of its next column are issued before the current column's P stores,
+// so the SM's loads do not stall behind a burst of stores.  All slots are free
+// by then: every copy has landed and every slot value has been folded.
 template <int DT, int OP, int ALGO, bool SCATTER, int THREADS>
 __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid_constant__ GenericParams p) {
   extern __shared__ uint4 slots[];                // [kSlots][THREADS]
@@ -218,42 +252,30 @@ __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid
 
   const uint64_t n = p.nfull;
   const uint64_t columns = n + (p.tail ? 1 : 0);
-  for (uint64_t v = (uint64_t)blockIdx.x * THREADS + tid; v < columns;
-       v += (uint64_t)gridDim.x * THREADS) {
-    const int t = (ALGO == kTree && v >= p.split) ? 1 : 0;
-    const int first = ALGO == kRing ? (int)(v / p.split) : 0;  // ring: chunk index = start rank
-    RankCursor<ALGO> cur;
-    cur.P = P;
-    cur.push = s_push[t];
-    if constexpr (ALGO == kRing) {
-      cur.a = first;
-    } else if constexpr (ALGO == kTree) {
-      cur.a = 0;
-    } else {
-      // hierarchical: intra-group chunk c1 (split = its length in vectors), then
-      // sub-chunk c2 of that chunk across the G groups
-      const uint64_t V = 16 / Lanes<DT>::kBytes;
-      const uint64_t c1 = v / p.split;
-      const uint64_t lo = c1 * p.split * V;
-      const uint64_t hi = lo + p.split * V < p.count ? lo + p.split * V : p.count;
-      const int G = P / p.Q;
-      const uint64_t L2v = ((hi - lo + G - 1) / G + V - 1) / V;
-      const uint64_t c2 = (v - c1 * p.split) / L2v;
-      cur.Q = p.Q;
-      cur.G = G;
-      cur.a0 = cur.a = (int)(c1 % (uint64_t)p.Q);
-      cur.b0 = cur.b = (int)c2;
-    }
-
-    Acc<DT> acc;
-    if (v < n) {
-      const uint32_t base = (uint32_t)__cvta_generic_to_shared(&slots[tid]);
-      constexpr uint32_t kSlotStride = THREADS * 16;
+  const uint64_t stride = (uint64_t)gridDim.x * THREADS;
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(&slots[tid]);
+  constexpr uint32_t kSlotStride = THREADS * 16;
+  // the first kWindow copies of column v, into slots 0 .. kWindow-1
+  auto prologue = [&](uint64_t v, RankCursor<ALGO>& cur) {
   #pragma unroll
-      for (int k = 0; k < kWindow; ++k) {
-        if (k < P) cp_async16(base + k * kSlotStride, s_send[cur.next()] + v);
-        cp_async_commit();
-      }
+    for (int k = 0; k < kWindow; ++k) {
+      if (k < P) cp_async16(base + k * kSlotStride, s_send[cur.next()] + v);
+      cp_async_commit();
+    }
+  };
+
+  uint64_t v = (uint64_t)blockIdx.x * THREADS + tid;
+  int first = 0;
+  RankCursor<ALGO> cur{};
+  if (v < columns) {
+    cur = column_cursor<DT, ALGO>(p, v, s_push, first);
+    if (v < n) prologue(v, cur);
+  }
+  for (; v < columns; v += stride) {
+    const uint64_t vn = v + stride;
+    int first_n = 0;
+    RankCursor<ALGO> cur_n = cur;
+    if (v < n) {
       int j = 0;          // values consumed
       int rd = 0;         // slot of value j
       int wr = kWindow;   // slot for value j + kWindow
@@ -268,21 +290,27 @@ __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid
         wr = wr + 1 == kSlots ? 0 : wr + 1;
         return widen<DT>(raw);
       };
-      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, next);
+      const Acc<DT> acc = fold_sequence<DT, OP, ALGO>(P, p.Q, next);
       cp_async_wait<0>();
       const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
+      if (vn < columns) {
+        cur_n = column_cursor<DT, ALGO>(p, vn, s_push, first_n);
+        if (vn < n) prologue(vn, cur_n);
+      }
       if constexpr (SCATTER) {
         st_stream(s_recv[first] + (v - (uint64_t)first * p.split), o);
       } else {
         for (int r = 0; r < P; ++r) st_stream(s_recv[r] + v, o);
       }
     } else {
-      // the trailing partial vector: element-wise loads, same order
+      // the trailing partial vector (the last column): element-wise loads, same order
       auto next = [&]() -> Acc<DT> { return widen<DT>(load_partial<DT>(s_send[cur.next()] + n, p.tail)); };
-      acc = fold_sequence<DT, OP, ALGO>(P, p.Q, next);
+      const Acc<DT> acc = fold_sequence<DT, OP, ALGO>(P, p.Q, next);
       const uint4 o = narrow<DT>(acc, p.scale, p.do_scale != 0);
       for (int r = 0; r < P; ++r) store_partial<DT>(s_recv[r] + n, o, p.tail);
     }
+    cur = cur_n;
+    first = first_n;
   }
 }
 

@@ -418,7 +418,7 @@ def test_capped_many_ranks(P, Q, dtype, dev, capfd):
                         want = oracle.allreduce_hier(sends, Q, dtype, op)
                     else:
                         want = oracle.allreduce(sends, dtype, op, oracle.TREE if algo == ar.AR_ALGO_TREE else oracle.RING)
-                    for r in (0, P - 1):
+                    for r in range(P):
                         assert outs[r].guards_intact()
                         pins.assert_bitwise(to_host(outs[r].tensor), want[r],
                                             f"P={P} dtype={dtype} count={count} op={op} algo={algo} rank={r}")
@@ -436,5 +436,41 @@ def test_capped_many_ranks(P, Q, dtype, dev, capfd):
         log = capfd.readouterr().err
         for k in ("wide_pipelined_ring", "wide_pipelined_tree", "wide_pipelined_hier", "wide_pipelined_reduce_scatter"):
             assert f"kernel={k} " in log, k
+    finally:
+        ar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("dtype", [ar.AR_BFLOAT16, ar.AR_INT32])
+def test_capped_many_ranks_long_grid_stride(dtype, dev):
+    """72 ranks on 16 SMs with about 21 column groups per block: the results
+    leave through the store warp's two alternating shared-memory buffers many
+    times over.  Every element of every rank against the oracle (every order,
+    the hierarchical one with groups of 8), out of place and in place."""
+    P, Q = 72, 8
+    V = VEC[dtype]
+    count = 21 * BLOCKS * 768 * V + 5 * V + 3
+    kind = "int" if dtype == ar.AR_INT32 else "normal_bf16"
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, Q)
+        sends = device_inputs(kind, 5, P, count, dev, 1e-3)
+        host = host_inputs(sends, kind, 5, 1e-3)
+        for algo, oalgo, group in ((ar.AR_ALGO_RING, oracle.RING, None), (ar.AR_ALGO_TREE, oracle.TREE, None),
+                                   (ar.AR_ALGO_HIER, None, Q)):
+            op = ar.AR_MAX if algo == ar.AR_ALGO_TREE else ar.AR_SUM
+            want = oracle_full(host, dtype, op, oalgo, 1.0, group=group)
+            outs = [torch.empty_like(s) for s in sends]
+            ar.ar_allreduce(comm, sends, outs, count, dtype, op, algo, 1.0)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            for r in range(P):
+                assert_equal_every_element(outs[r], want, f"algo={algo} rank {r}")
+            inplace = [s.clone() for s in sends]
+            ar.ar_allreduce(comm, inplace, inplace, count, dtype, op, algo, 1.0)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            for r in range(P):
+                assert torch.equal(inplace[r], outs[r]), f"in place, algo={algo} rank {r}"
     finally:
         ar.ar_destroy(comm)
