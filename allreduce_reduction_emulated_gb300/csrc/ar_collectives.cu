@@ -53,6 +53,7 @@ __device__ __forceinline__ void store_elem(void* base, uint64_t e, typename Lane
 // order of chunk s (x_s, x_{s+1}, ...), result to rank s at e - s * shard.
 template <int DT, int OP>
 __global__ void __launch_bounds__(kThreads) reduce_scatter_elem_kernel(const __grid_constant__ CollParams p) {
+  pdl_enter();
   __shared__ const void* s_send[AR_MAX_RANKS];
   for (int r = threadIdx.x; r < p.P; r += kThreads) s_send[r] = p.send[r];
   __syncthreads();
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) reduce_scatter_elem_kernel(const __g
 
 // Vector v of the P * (shard / V) source vectors: rank s = v / (shard / V).
 __global__ void __launch_bounds__(kThreads) all_gather_vec_kernel(const __grid_constant__ CollParams p) {
+  pdl_enter();
   __shared__ uint4* s_recv[AR_MAX_RANKS];
   for (int r = threadIdx.x; r < p.P; r += kThreads) s_recv[r] = static_cast<uint4*>(p.recv[r]);
   __syncthreads();
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) all_gather_vec_kernel(const __grid_c
 
 template <typename W>
 __global__ void __launch_bounds__(kThreads) all_gather_elem_kernel(const __grid_constant__ CollParams p) {
+  pdl_enter();
   __shared__ W* s_recv[AR_MAX_RANKS];
   for (int r = threadIdx.x; r < p.P; r += kThreads) s_recv[r] = static_cast<W*>(p.recv[r]);
   __syncthreads();
@@ -119,10 +122,11 @@ void fill(CollParams& p, const Call& c) {
 template <int DT>
 cudaError_t launch_rs_elem_dt(const Call& c, CollParams& p) {
   const unsigned g = grid_for(p.total, c.max_blocks);
+  const bool pdl = use_pdl(c);
   switch (c.op) {
-    case kSum: reduce_scatter_elem_kernel<DT, kSum><<<g, kThreads, 0, c.stream>>>(p); break;
-    case kMin: reduce_scatter_elem_kernel<DT, kMin><<<g, kThreads, 0, c.stream>>>(p); break;
-    case kMax: reduce_scatter_elem_kernel<DT, kMax><<<g, kThreads, 0, c.stream>>>(p); break;
+    case kSum: (void)launch_kernel(reduce_scatter_elem_kernel<DT, kSum>, dim3(g), dim3(kThreads), 0, c.stream, pdl, p); break;
+    case kMin: (void)launch_kernel(reduce_scatter_elem_kernel<DT, kMin>, dim3(g), dim3(kThreads), 0, c.stream, pdl, p); break;
+    case kMax: (void)launch_kernel(reduce_scatter_elem_kernel<DT, kMax>, dim3(g), dim3(kThreads), 0, c.stream, pdl, p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -154,14 +158,14 @@ cudaError_t launch_all_gather(const Call& c, LaunchInfo* info) {
     p.shard = c.shard * es / 16;  // vectors per shard
     p.total = (uint64_t)c.P * p.shard;
     const unsigned g = grid_for(p.total, c.max_blocks);
-    all_gather_vec_kernel<<<g, kThreads, 0, c.stream>>>(p);
+    (void)launch_kernel(all_gather_vec_kernel, dim3(g), dim3(kThreads), 0, c.stream, use_pdl(c), p);
     info->kernel = "all_gather_vec";
     info->grid = (int)g;
   } else {
     p.total = (uint64_t)c.P * c.shard;
     const unsigned g = grid_for(p.total, c.max_blocks);
-    if (es == 2) all_gather_elem_kernel<uint16_t><<<g, kThreads, 0, c.stream>>>(p);
-    else all_gather_elem_kernel<uint32_t><<<g, kThreads, 0, c.stream>>>(p);
+    if (es == 2) (void)launch_kernel(all_gather_elem_kernel<uint16_t>, dim3(g), dim3(kThreads), 0, c.stream, use_pdl(c), p);
+    else (void)launch_kernel(all_gather_elem_kernel<uint32_t>, dim3(g), dim3(kThreads), 0, c.stream, use_pdl(c), p);
     info->kernel = "all_gather_elem";
     info->grid = (int)g;
   }

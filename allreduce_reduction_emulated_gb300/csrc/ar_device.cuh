@@ -24,6 +24,19 @@ template <int DT> struct Acc {
   typename Lanes<DT>::T v[Lanes<DT>::N];
 };
 
+// ----------------------------------------------------------------- launch order
+
+// Every kernel starts here.  Launched with programmatic dependent launch
+// (launch_kernel), a kernel may be scheduled while the kernel before it on the
+// stream is still draining; it first lets its own successor be scheduled the
+// same way, then waits until its predecessor has completed and that kernel's
+// writes are visible, before it touches memory.  Launched plainly, or with no
+// kernel before it, the wait returns at once.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- memory
 
 // Cache hints of the streaming accesses (compile-time tunables).

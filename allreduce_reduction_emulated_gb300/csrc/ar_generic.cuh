@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid
   __shared__ const uint4* s_send[AR_MAX_RANKS];
   __shared__ uint4* s_recv[AR_MAX_RANKS];
   __shared__ int16_t s_push[2][AR_MAX_RANKS];   // tree leaf (push) sequences
+  pdl_enter();
   const int P = p.P;
   const int tid = threadIdx.x;
   for (int r = tid; r < P; r += THREADS) {
@@ -368,7 +369,7 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
   static std::atomic<uint64_t> configured{0};
   cudaError_t e = opt_in_smem(kernel, kSmem, configured);
   if (e != cudaSuccess) return e;
-  kernel<<<(unsigned)grid, THREADS, kSmem, c.stream>>>(p);
+  (void)launch_kernel(kernel, dim3((unsigned)grid), dim3(THREADS), kSmem, c.stream, use_pdl(c), p);
   const bool wide = THREADS != kThreads;
   info->kernel = ALGO == kRing ? (wide ? "wide_pipelined_ring" : "pipelined_ring")
                  : ALGO == kHier ? (wide ? "wide_pipelined_hier" : "pipelined_hier")
@@ -422,7 +423,7 @@ cudaError_t launch_scatter_one(const Call& c, LaunchInfo* info) {
   static std::atomic<uint64_t> configured{0};
   cudaError_t e = opt_in_smem(kernel, kSmem, configured);
   if (e != cudaSuccess) return e;
-  kernel<<<(unsigned)grid, THREADS, kSmem, c.stream>>>(p);
+  (void)launch_kernel(kernel, dim3((unsigned)grid), dim3(THREADS), kSmem, c.stream, use_pdl(c), p);
   info->kernel = THREADS != kThreads ? "wide_pipelined_reduce_scatter" : "pipelined_reduce_scatter";
   info->grid = (int)grid;
   info->block = THREADS;

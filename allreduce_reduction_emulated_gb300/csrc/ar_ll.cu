@@ -156,6 +156,7 @@ __device__ __forceinline__ void ll_reduce_slice(const LLParams<MAXP>& p, uint64_
 
 template <int MAXP, int DT, int OP>
 __global__ void __launch_bounds__(kLLBlock) ll_allreduce_kernel(const __grid_constant__ LLParams<MAXP> p) {
+  pdl_enter();
   const bool worker = threadIdx.x < kLLThreads;
   const uint64_t base = (uint64_t)blockIdx.x * (uint64_t)p.slice_words;
   const uint64_t left = p.nwords - base;
@@ -239,7 +240,7 @@ cudaError_t launch_ll_one(const Call& c, LaunchInfo* info) {
   p.slice_words = (int)slice;
   const uint64_t grid = (p.nwords + slice - 1) / slice;
   if (grid == 0 || grid > 0x7fffffffull) return cudaErrorInvalidValue;
-  kernel<<<(unsigned)grid, kLLBlock, 0, c.stream>>>(p);
+  (void)launch_kernel(kernel, dim3((unsigned)grid), dim3(kLLBlock), 0, c.stream, use_pdl(c), p);
   const cudaError_t e = cudaGetLastError();
   info->kernel = "ll";
   info->grid = (int)grid;

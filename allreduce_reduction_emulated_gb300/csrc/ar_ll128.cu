@@ -183,6 +183,7 @@ __device__ __forceinline__ void ll128_reduce_slice(const LL128Params<MAXP>& p, u
 
 template <int MAXP, int DT, int OP>
 __global__ void __launch_bounds__(kBlock) ll128_allreduce_kernel(const __grid_constant__ LL128Params<MAXP> p) {
+  pdl_enter();
   const bool worker = threadIdx.x < kThreads;
   const int lane = threadIdx.x & 31;
   const int part = lane & 7;  // 16-byte part of a line
@@ -276,7 +277,7 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   p.slice_lines = (int)slice;
   const uint64_t grid = (p.nlines + slice - 1) / slice;
   if (grid == 0 || grid > 0x7fffffffull) return cudaErrorInvalidValue;
-  kernel<<<(unsigned)grid, kBlock, 0, c.stream>>>(p);
+  (void)launch_kernel(kernel, dim3((unsigned)grid), dim3(kBlock), 0, c.stream, use_pdl(c), p);
   const cudaError_t e = cudaGetLastError();
   info->kernel = "ll128";
   info->grid = (int)grid;

@@ -108,6 +108,7 @@ template <int NP, int DT, int OP, int ALGO, bool SCATTER = false, int THREADS = 
           int U = kStaticUnroll>
 __global__ void __launch_bounds__(THREADS)
     static_allreduce_kernel(const __grid_constant__ StaticParams<NP> p) {
+  pdl_enter();
   const uint64_t n = p.nfull;
   const uint64_t step = (uint64_t)gridDim.x * (THREADS * U);
   for (uint64_t base = (uint64_t)blockIdx.x * (THREADS * U) + threadIdx.x; base < n;
@@ -181,7 +182,7 @@ cudaError_t launch_static_one(const Call& c, LaunchInfo* info) {
   uint64_t cap = kStaticPersistent || WIDE ? (uint64_t)c.sms * (uint64_t)blocks_per_sm : 0x7fffffffull;
   if (c.max_blocks > 0 && (uint64_t)c.max_blocks < cap) cap = (uint64_t)c.max_blocks;
   const int grid = (int)(need < 1 ? 1 : (need < cap ? need : cap));
-  kernel<<<grid, kThreads, 0, c.stream>>>(p);
+  (void)launch_kernel(kernel, dim3((unsigned)grid), dim3(kThreads), 0, c.stream, use_pdl(c), p);
   info->kernel = WIDE ? (SCATTER ? "wide_reduce_scatter" : ALGO == kRing ? "wide_ring" : "wide_tree")
                       : (SCATTER ? "static_reduce_scatter" : ALGO == kRing ? "static_ring" : "static_tree");
   info->grid = grid;

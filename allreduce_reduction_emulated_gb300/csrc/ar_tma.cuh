@@ -140,6 +140,7 @@ __device__ __forceinline__ uint4 fold_column(const uint4 (&r)[NP], int order, ui
 
 template <int NP, int DT, int OP, int ALGO, bool SCATTER = false>
 __global__ void __launch_bounds__(Shape<SCATTER, DT>::kThreads, 1) allreduce_kernel(const __grid_constant__ Params<NP> p) {
+  pdl_enter();
   constexpr int kTile = Shape<SCATTER, DT>::kTile;
   constexpr int kStages = Shape<SCATTER, DT>::kStages;
   constexpr int kConsumerWarps = Shape<SCATTER, DT>::kConsumerWarps;
@@ -305,7 +306,7 @@ cudaError_t launch_one(const Call& c, LaunchInfo* info) {
   if (grid > (uint64_t)c.sms) grid = (uint64_t)c.sms;  // one block per SM
   if (grid > p.ntiles) grid = p.ntiles;
   if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, Shape<SCATTER, DT>::kThreads, kSmem, c.stream>>>(p);
+  (void)launch_kernel(kernel, dim3((unsigned)grid), dim3(Shape<SCATTER, DT>::kThreads), kSmem, c.stream, use_pdl(c), p);
   info->kernel = SCATTER ? "tma_reduce_scatter" : ALGO == kRing ? "tma_ring" : "tma_tree";
   info->grid = (int)grid;
   info->block = Shape<SCATTER, DT>::kThreads;

@@ -33,6 +33,7 @@ struct GatherParams {
 };
 
 __global__ void __launch_bounds__(32, 1) all_gather_tma_kernel(const __grid_constant__ GatherParams p) {
+  pdl_enter();
   extern __shared__ __align__(128) char smem[];
   __shared__ __align__(8) uint64_t full[kGatherStages];
   if (threadIdx.x != 0) return;
@@ -111,7 +112,7 @@ cudaError_t launch_all_gather_tma(const Call& c, LaunchInfo* info) {
   if (grid > (uint64_t)c.sms) grid = (uint64_t)c.sms;
   if (grid > ntiles) grid = ntiles;
   if (grid < 1) grid = 1;
-  all_gather_tma_kernel<<<(unsigned)grid, 32, kGatherSmem, c.stream>>>(p);
+  (void)launch_kernel(all_gather_tma_kernel, dim3((unsigned)grid), dim3(32), kGatherSmem, c.stream, use_pdl(c), p);
   info->kernel = "tma_all_gather";
   info->grid = (int)grid;
   info->block = 32;

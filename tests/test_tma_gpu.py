@@ -474,3 +474,44 @@ def test_capped_many_ranks_long_grid_stride(dtype, dev):
                 assert torch.equal(inplace[r], outs[r]), f"in place, algo={algo} rank {r}"
     finally:
         ar.ar_destroy(comm)
+
+
+def test_capped_at_the_rank_limit(dev):
+    """AR_MAX_RANKS ranks on 16 SMs (the 768-thread pipelined kernel at its
+    largest rank count): ring, tree, hierarchical (groups of 16) and the
+    reduce-scatter, every element of every rank against the oracle."""
+    P, Q, dtype = ar.AR_MAX_RANKS, 16, ar.AR_INT32
+    V = VEC[dtype]
+    count = 2 * BLOCKS * 768 * V + 3 * V + 2
+    rng = np.random.default_rng(4100)
+    comm = ar.ar_init(P)
+    try:
+        ar.ar_set_option(comm, ar.AR_OPT_MAX_BLOCKS, BLOCKS)
+        ar.ar_set_option(comm, ar.AR_OPT_HIER_GROUP, Q)
+        sends = pins.random_inputs(rng, P, count, dtype)
+        xs = [to_device(a, dtype, dev) for a in sends]
+        for algo, op in ((ar.AR_ALGO_RING, ar.AR_SUM), (ar.AR_ALGO_TREE, ar.AR_SUM), (ar.AR_ALGO_HIER, ar.AR_MIN)):
+            outs = [Guarded(count, dtype, dev) for _ in range(P)]
+            ar.ar_allreduce(comm, xs, [o.tensor for o in outs], count, dtype, op, algo, 1.0)
+            torch.cuda.synchronize()
+            assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+            if algo == ar.AR_ALGO_HIER:
+                want = oracle.allreduce_hier(sends, Q, dtype, op)
+            else:
+                want = oracle.allreduce(sends, dtype, op, oracle.TREE if algo == ar.AR_ALGO_TREE else oracle.RING)
+            for r in range(P):
+                assert outs[r].guards_intact()
+                pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"P={P} algo={algo} rank={r}")
+        rc = 64 * V + V
+        sends = pins.random_inputs(rng, P, P * rc, dtype)
+        xs = [to_device(a, dtype, dev) for a in sends]
+        outs = [Guarded(rc, dtype, dev) for _ in range(P)]
+        ar.ar_reduce_scatter(comm, xs, [o.tensor for o in outs], rc, dtype, ar.AR_SUM, 1.0)
+        torch.cuda.synchronize()
+        assert ar.ar_get_status(comm) == ar.AR_SUCCESS
+        want = oracle.reduce_scatter(sends, dtype, oracle.SUM, 1.0)
+        for r in range(P):
+            assert outs[r].guards_intact()
+            pins.assert_bitwise(to_host(outs[r].tensor), want[r], f"RS P={P} rank={r}")
+    finally:
+        ar.ar_destroy(comm)
