@@ -228,6 +228,17 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.rows.append((time.time(), [f.strip() for f in line.split(",")]))
 
+    def wait_fresh_row(self, limit_s: float = 0.25):
+        """Returns right after nvidia-smi has printed a row (or after limit_s).
+        A timed region started then ends long before nvidia-smi's next query
+        (every 50 ms), so the in-process NVML reads are not held up behind it."""
+        if self.proc is None:
+            return
+        n = len(self.rows)
+        t_end = time.time() + limit_s
+        while len(self.rows) == n and time.time() < t_end:
+            time.sleep(0.0002)
+
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -352,10 +363,12 @@ HIDE_CYCLES = 4_000_000   # ~2 ms at 2 GHz
 
 
 def timed_steps(torch, step, steps: int, stream, nvml: "NvmlClocks | None" = None,
-                range_name: str = "timed") -> float:
+                range_name: str = "timed", clocks: "ClockSampler | None" = None) -> float:
     """ms for `steps` calls of step(), timed by CUDA events on `stream`."""
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    if clocks is not None:
+        clocks.wait_fresh_row()
     with torch.cuda.stream(stream):
         torch.cuda._sleep(HIDE_CYCLES)
     torch.cuda.nvtx.range_push(range_name)   # lets a profiler select exactly this region
@@ -640,7 +653,7 @@ def ours_arm(args, w, name):
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    ms = timed_steps(torch, step, args.steps, stream, nvml)
+    ms = timed_steps(torch, step, args.steps, stream, nvml, clocks=clocks)
     t1 = time.time()
     if dist:
         dist.barrier()
@@ -1001,7 +1014,7 @@ def ddp_buckets(args):
         g.replay()
     torch.cuda.synchronize()
     t0 = time.time()
-    graph_ms = timed_steps(torch, g.replay, args.steps, stream, nvml) / args.steps
+    graph_ms = timed_steps(torch, g.replay, args.steps, stream, nvml, clocks=clocks) / args.steps
     t1 = time.time()
     time.sleep(0.2)
     clocks.stop()

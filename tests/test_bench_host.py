@@ -116,6 +116,26 @@ def test_clock_summary_reads_nvidia_smi_rows():
     assert s["samples_in_timed_region"] == 0 and s["samples"] == 7 and s["sm_mhz"] == 2017.5  # median of 6
 
 
+def test_timed_region_starts_right_after_an_nvidia_smi_row():
+    """The timed region waits for nvidia-smi's next row, so the region (a few
+    ms) ends before nvidia-smi's following query; without nvidia-smi, or once
+    the wait's limit has passed, it starts at once."""
+    import threading
+    import time
+
+    c = bench.ClockSampler(0)
+    c.wait_fresh_row()                                   # no nvidia-smi process: no wait
+    c.proc = object()
+    t0 = time.time()
+    threading.Timer(0.05, lambda: c.rows.append((time.time(), ["0"]))).start()
+    c.wait_fresh_row(limit_s=2.0)
+    waited = time.time() - t0
+    assert len(c.rows) == 1 and 0.04 <= waited < 1.0
+    t0 = time.time()
+    c.wait_fresh_row(limit_s=0.05)                       # no new row: gives up at the limit
+    assert 0.04 <= time.time() - t0 < 1.0
+
+
 def test_overlap_arguments(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py", "--ddp-overlap", "--comm-blocks", "auto", "--gemm-carveout", "32",
                                      "--grad-dtype", "bf16", "--comm-priority"])
