@@ -140,6 +140,15 @@ ar_status_t ar_init(int nranks, ar_comm_t* out);
  * AR_ERR_UNSUPPORTED) before anything is enqueued; launch failures return
  * AR_ERR_CUDA; device-side errors (a wait limit) are reported later by
  * ar_get_status.
+ * Launch order: a call without an SM cap (AR_OPT_MAX_BLOCKS) is launched with
+ * programmatic dependent launch, so its kernel may become resident while the
+ * kernel before it on `stream` drains; it waits on the device until that
+ * kernel has completed and its writes are visible before it reads or writes
+ * any buffer, so the stream's order holds.  Every kernel of the library also
+ * lets the kernel after it start early the same way: a kernel of the caller's
+ * that is launched with programmatic stream serialization after a call must
+ * wait (cudaGridDependencySynchronize) before it reads the call's results,
+ * as the CUDA programming model requires of any such kernel.
  * CUDA graphs: every algorithm may be captured and replayed (the buffers
  * are then fixed).  The LL / LL128 epoch lives in device memory and each
  * launch takes the next value itself, so a replayed call never matches an
