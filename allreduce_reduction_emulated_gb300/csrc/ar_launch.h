@@ -57,7 +57,8 @@ struct LaunchInfo {
 // memory, so the stream's order is kept and only the launch gap is hidden
 // (8 x 64 MiB fp32 ring: 157.7 -> 155.0 us per call back to back).  A call
 // capped to a few SMs is launched plainly: its blocks would otherwise wait on
-// SMs that other work is using.
+// SMs that other work is using (bucket all-reduces on 48 SMs beside gradient
+// GEMMs: 27.05 ms per step launched this way, 25.01 ms plainly).
 inline bool use_pdl(const Call& c) { return c.max_blocks <= 0 || c.max_blocks >= c.sms; }
 
 template <class... K, class... A>
