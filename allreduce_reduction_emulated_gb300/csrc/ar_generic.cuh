@@ -1,9 +1,9 @@
 // ar_generic.cuh -- ring-order and tree-order all-reduce for any rank count up
 // to AR_MAX_RANKS (used above the rank-specialised kernels' limit), templated
-// on the block width: 128 threads (ar_generic.cu) for calls with the whole
+// on the block width: 64 threads (ar_generic.cu) for calls with the whole
 // GPU, 768 threads, one block per SM (ar_generic_wide.cu), for calls capped to
-// a few SMs (AR_OPT_MAX_BLOCKS), where 128-thread blocks left each SM with too
-// few copies in flight (2.5 TB/s for 72 ranks on 48 SMs).
+// a few SMs (AR_OPT_MAX_BLOCKS), where small blocks left each SM with too few
+// copies in flight (2.5 TB/s for 72 ranks on 48 SMs in 128-thread blocks).
 //
 // With many ranks the P input vectors of a column no longer fit in registers,
 // and the fold order needs a dynamic rank index.  Each thread owns one column
@@ -31,16 +31,26 @@ namespace ar {
 namespace {
 
 #ifndef AR_GENERIC_WINDOW
-#define AR_GENERIC_WINDOW 16
+#define AR_GENERIC_WINDOW 24
 #endif
 #ifndef AR_GENERIC_THREADS
-#define AR_GENERIC_THREADS 128
+#define AR_GENERIC_THREADS 64
 #endif
 
-constexpr int kWindow = AR_GENERIC_WINDOW;    // copies in flight per thread
-constexpr int kSlots = kWindow + 1;           // one spare slot between read and refill
+// With the whole GPU: 64-thread blocks, 24 copies in flight per thread (25
+// slots, 25.6 KiB per block, 8 blocks per SM).  The same copies in flight per
+// SM as 128 threads x 16 but shorter chains per column, so the last wave
+// drains sooner: 72 x 4 / 16 MiB int32 ring 92.7 / 350.0 us against
+// 94.1 / 353.6 (back to back).  Under a cap: 768 threads, 16 in flight
+// (17 x 768 x 16 B = 204 KiB of slots, one block per SM).
+constexpr int kWindow = AR_GENERIC_WINDOW;    // copies in flight per thread, whole GPU
 constexpr int kThreads = AR_GENERIC_THREADS;  // block width with the whole GPU
-constexpr int kWideThreads = 768;             // block width under a cap: 17 x 768 x 16 B = 204 KiB of slots
+constexpr int kWideThreads = 768;             // block width under a cap
+constexpr int kWideWindow = 16;               // copies in flight per thread under a cap
+template <int THREADS>
+__host__ __device__ constexpr int window_of() { return THREADS == kWideThreads ? kWideWindow : kWindow; }
+template <int THREADS>
+__host__ __device__ constexpr int slots_of() { return window_of<THREADS>() + 1; }  // one spare slot between read and refill
 constexpr int kStackDepth = 16;               // >= tree height + 1 for P <= AR_MAX_RANKS
 
 struct GenericParams {
@@ -234,6 +244,8 @@ __device__ __forceinline__ RankCursor<ALGO> column_cursor(const GenericParams& p
 // by then: every copy has landed and every slot value has been folded.
 template <int DT, int OP, int ALGO, bool SCATTER, int THREADS>
 __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid_constant__ GenericParams p) {
+  constexpr int kWin = window_of<THREADS>();
+  constexpr int kSlots = slots_of<THREADS>();
   extern __shared__ uint4 slots[];                // [kSlots][THREADS]
   __shared__ const uint4* s_send[AR_MAX_RANKS];
   __shared__ uint4* s_recv[AR_MAX_RANKS];
@@ -256,10 +268,10 @@ __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid
   const uint64_t stride = (uint64_t)gridDim.x * THREADS;
   const uint32_t base = (uint32_t)__cvta_generic_to_shared(&slots[tid]);
   constexpr uint32_t kSlotStride = THREADS * 16;
-  // the first kWindow copies of column v, into slots 0 .. kWindow-1
+  // the first kWin copies of column v, into slots 0 .. kWin-1
   auto prologue = [&](uint64_t v, RankCursor<ALGO>& cur) {
   #pragma unroll
-    for (int k = 0; k < kWindow; ++k) {
+    for (int k = 0; k < kWin; ++k) {
       if (k < P) cp_async16(base + k * kSlotStride, s_send[cur.next()] + v);
       cp_async_commit();
     }
@@ -279,11 +291,11 @@ __global__ void __launch_bounds__(THREADS) generic_allreduce_kernel(const __grid
     if (v < n) {
       int j = 0;          // values consumed
       int rd = 0;         // slot of value j
-      int wr = kWindow;   // slot for value j + kWindow
+      int wr = kWin;      // slot for value j + kWin
       auto next = [&]() -> Acc<DT> {
-        cp_async_wait<kWindow - 1>();  // value j has landed
+        cp_async_wait<kWin - 1>();  // value j has landed
         const uint4 raw = slots[rd * THREADS + tid];
-        const int k = j + kWindow;
+        const int k = j + kWin;
         if (k < P) cp_async16(base + wr * kSlotStride, s_send[cur.next()] + v);
         cp_async_commit();
         ++j;
@@ -365,7 +377,7 @@ cudaError_t launch_generic_one(const Call& c, LaunchInfo* info) {
   const uint64_t columns = p.nfull + (p.tail ? 1 : 0);
   const uint64_t grid = generic_grid<THREADS>(columns, c);
   if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
-  constexpr size_t kSmem = sizeof(uint4) * kSlots * THREADS;
+  constexpr size_t kSmem = sizeof(uint4) * slots_of<THREADS>() * THREADS;
   static std::atomic<uint64_t> configured{0};
   cudaError_t e = opt_in_smem(kernel, kSmem, configured);
   if (e != cudaSuccess) return e;
@@ -419,7 +431,7 @@ cudaError_t launch_scatter_one(const Call& c, LaunchInfo* info) {
   p.do_scale = (DT != kI32 && c.scale != 1.0f) ? 1 : 0;
   const uint64_t grid = generic_grid<THREADS>(p.nfull, c);
   if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
-  constexpr size_t kSmem = sizeof(uint4) * kSlots * THREADS;
+  constexpr size_t kSmem = sizeof(uint4) * slots_of<THREADS>() * THREADS;
   static std::atomic<uint64_t> configured{0};
   cudaError_t e = opt_in_smem(kernel, kSmem, configured);
   if (e != cudaSuccess) return e;
