@@ -86,6 +86,13 @@ def test_traffic_only_while_the_sources_match(monkeypatch):
     assert bench.profiled_traffic("no_such_workload") is None
 
 
+def test_every_summary_matches_the_current_kernel_sources():
+    """A kernel edited after its ncu capture makes bench.py report no traffic
+    for it; this names such a summary, so it is re-captured with the change."""
+    stale = [w for w in bench.PROFILES if bench.profiled_traffic(w) is None]
+    assert stale == [], f"re-capture the ncu summaries of {stale}"
+
+
 def test_oracle_timing_runs_on_one_core():
     import os
 
