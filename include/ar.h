@@ -227,7 +227,8 @@ typedef enum {
                                     run the kernel AR_OPT_CAPPED_KERNEL names,
                                     one block per SM (the TMA pipeline needs at
                                     least 4 KiB per rank per block, else the
-                                    256-thread load/store kernel runs); more
+                                    whole-GPU load/store kernel runs, capped);
+                                    more
                                     ranks, and the hierarchical order, run the
                                     pipelined kernel in 768-thread blocks, one
                                     per SM; all-gathers of whole 16-byte pieces
