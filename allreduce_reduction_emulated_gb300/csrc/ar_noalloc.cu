@@ -50,8 +50,8 @@ DeviceState g_state[kMaxDevices];
 
 // Per device, with that device current: the array's device address.  (In
 // host code the symbol names a host-side stand-in, not device memory.)  A
-// lookup that fails -- for example one attempted while the stream is being
-// captured -- leaves the device not ready, and the next call tries again.
+// lookup that fails leaves the device not ready, and the next call tries
+// again.
 cudaError_t set_up(DeviceState& s, int dev) {
   if (s.ready.load(std::memory_order_acquire)) return cudaSuccess;
   std::lock_guard<std::mutex> lock(s.mu);

@@ -339,9 +339,8 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* sendbufs, void* con
  *                 AR_ERR_TIMEOUT (a flag wait ran out in this or an earlier
  *                 call on this device) and clears the device status word.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before capturing any stream.  If that
- * lookup fails (AR_ERR_CUDA, for example when it is attempted during a
- * capture), nothing is cached: the next call on the device tries again.  Every call
+ * device current.  If that lookup fails (AR_ERR_CUDA), nothing is cached: the
+ * next call on the device tries again.  Every call
  * on a device shares the one array: calls that overlap on the GPU (for example
  * on two streams at once) race and must not be issued.
  * Errors: AR_ERR_INVALID_ARG (bad pointer, alignment, overlap, enum, NaN
